@@ -1,0 +1,137 @@
+"""Seeded synthetic operands for D = A·Bᵀ (fp16 A [M,K], fp16 B [N,K]).
+
+This module draws numbers and nothing else: it holds none of the GEMM's
+arithmetic, so both the CPU oracle and the CUDA path may take their inputs
+from it.  Values are drawn in float64 from NumPy's PCG64 generator
+(``numpy.random.default_rng(seed)``) and rounded to fp16 by NumPy's own
+float64→float16 cast (round to nearest, ties to even).
+
+The five named workloads follow the shapes and value distributions the pages
+work with: the single 128×128 output tile with K=64 of "Building a Tiled
+GEMM" (MLC), step 1; its multi-tile K-loop (steps 2 and 3); the 8192³ fp16
+problem of the Croqtile tutorial ("dense GEMM fp16 from naive", headline
+table); a ragged shape with no dimension a multiple of 128; and the small-
+batch decode shape the blog post's "small batch" pitfall (§5.4) is about.
+"Normal(0, 1/√K)" is read as standard deviation 1/√K.  B's seed is A's seed
+plus 1000.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+_CHUNK = 1 << 22  # elements drawn per generator call (bounds float64 scratch)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dist_a: str      # "uniform" (U[-1,1]) or "normal:<sigma>" or "normal:1/sqrtK"
+    dist_b: str
+    seed: int        # seed of A; B uses seed + 1000
+
+    @property
+    def seed_b(self) -> int:
+        return self.seed + 1000
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def compulsory_bytes(self) -> int:
+        """A and B read once, D written once (fp16 = 2 bytes each)."""
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+
+WORKLOADS = {
+    w.name: w for w in (
+        Workload("single_tile_128x128x64", 128, 128, 64, "uniform", "uniform", 1),
+        Workload("multi_tile_1024x1024x2048", 1024, 1024, 2048, "uniform", "uniform", 2),
+        Workload("square_8192x8192x8192", 8192, 8192, 8192, "normal:1/sqrtK", "normal:1/sqrtK", 3),
+        Workload("ragged_4000x11000x4104", 4000, 11000, 4104, "uniform", "uniform", 4),
+        Workload("skinny_16x8192x8192", 16, 8192, 8192, "normal:1", "normal:1/sqrtK", 5),
+    )
+}
+
+#: the workload the headline throughput is quoted on
+HEADLINE = "square_8192x8192x8192"
+
+
+def _sigma(dist: str, K: int) -> float:
+    arg = dist.split(":", 1)[1]
+    if arg == "1/sqrtK":
+        return 1.0 / math.sqrt(K)
+    return float(arg)
+
+
+def draw(rows: int, cols: int, dist: str, seed: int, K: int | None = None,
+         chunk: int = _CHUNK) -> np.ndarray:
+    """A C-contiguous float16 [rows, cols] array of i.i.d. draws.
+
+    ``dist`` is "uniform" (U[-1, 1]) or "normal:<sigma>" where sigma is a
+    number or "1/sqrtK".  Draws are made in chunks from one generator, which
+    gives the same stream as a single call.
+    """
+    K = cols if K is None else K
+    rng = np.random.default_rng(seed)
+    total = rows * cols
+    out = np.empty(total, dtype=np.float16)
+    if dist == "uniform":
+        gen = lambda n: rng.uniform(-1.0, 1.0, n)          # noqa: E731
+    elif dist.startswith("normal:"):
+        sigma = _sigma(dist, K)
+        gen = lambda n: rng.normal(0.0, sigma, n)           # noqa: E731
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    for start in range(0, total, chunk):
+        n = min(chunk, total - start)
+        out[start:start + n] = gen(n).astype(np.float16)
+    return out.reshape(rows, cols)
+
+
+def operands(M: int, N: int, K: int, dist_a: str = "uniform", dist_b: str = "uniform",
+             seed: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """(A [M,K], B [N,K]) float16, A from ``seed`` and B from ``seed + 1000``."""
+    A = draw(M, K, dist_a, seed, K=K)
+    B = draw(N, K, dist_b, seed + 1000, K=K)
+    return A, B
+
+
+def workload_operands(name: str) -> tuple[np.ndarray, np.ndarray]:
+    w = WORKLOADS[name]
+    return operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
+
+
+def sample_entries(M: int, N: int, seed: int, n_rows: int = 8, n_cols: int = 8,
+                   n_random: int = 65536, extra_rows=(), extra_cols=()):
+    """Seeded (row, col) index pairs for checking a large D entry by entry.
+
+    All of ``n_rows`` seeded rows (every column), all of ``n_cols`` seeded
+    columns (every row), ``n_random`` seeded random entries, the four corners,
+    and every entry of the rows/columns listed in ``extra_rows``/``extra_cols``
+    (the last row and column of partial tiles, say).  Returns two int64
+    arrays; pairs may repeat.
+    """
+    rng = np.random.default_rng(seed)
+    rows = [rng.integers(0, M, n_rows), np.asarray(list(extra_rows), dtype=np.int64)]
+    cols = [rng.integers(0, N, n_cols), np.asarray(list(extra_cols), dtype=np.int64)]
+    sel_rows = np.unique(np.concatenate(rows).astype(np.int64))
+    sel_cols = np.unique(np.concatenate(cols).astype(np.int64))
+    r_parts, c_parts = [], []
+    for r in sel_rows:
+        r_parts.append(np.full(N, r, dtype=np.int64))
+        c_parts.append(np.arange(N, dtype=np.int64))
+    for c in sel_cols:
+        r_parts.append(np.arange(M, dtype=np.int64))
+        c_parts.append(np.full(M, c, dtype=np.int64))
+    r_parts.append(rng.integers(0, M, n_random).astype(np.int64))
+    c_parts.append(rng.integers(0, N, n_random).astype(np.int64))
+    r_parts.append(np.array([0, 0, M - 1, M - 1], dtype=np.int64))
+    c_parts.append(np.array([0, N - 1, 0, N - 1], dtype=np.int64))
+    return np.concatenate(r_parts), np.concatenate(c_parts)

@@ -1,0 +1,235 @@
+/*
+ * gemm_oracle.c -- the CPU oracle for the dense fp16 GEMM  D = A * B^T.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  The CUDA library
+ * never links, loads or calls it, and it shares no code with that library.
+ *
+ * What it computes (and where the definition comes from):
+ *   "Building a Tiled GEMM" (MLC, Modern GPU Programming for MLSys),
+ *   section "GEMM": A is M x K, B is N x K (the linear-layer weight layout,
+ *   read as stored, never transposed), D is M x N and
+ *       D[m,n] = sum_k A[m,k] * B[n,k].
+ *   Same section: A, B and D are stored as fp16 and the MMA accumulates in
+ *   fp32.  The oracle is the plain definition at higher precision:
+ *       D[m,n] = fp16_rne( sum_{k=0}^{K-1} (double)A[m,k] * (double)B[n,k] )
+ *   summed in ascending k with one fp64 accumulator, then rounded ONCE,
+ *   directly from fp64 to fp16 (round to nearest, ties to even).  The
+ *   product of two fp16 values has at most 22 significant bits, so every
+ *   product is exact in fp64; contraction into an FMA would not change it,
+ *   and the build passes -ffp-contract=off anyway.
+ *
+ * Readings of the pages taken here (the pages leave them open):
+ *   - the rounding mode of the final fp32->fp16 cast is not stated on the
+ *     pages; round-to-nearest-even (the IEEE default) is used;
+ *   - a K that is not a multiple of the 64-wide K tile still contributes
+ *     every k (the definition sums over all k);
+ *   - NaN and infinity inputs follow IEEE arithmetic in fp64.
+ *
+ * Binary16 (IEEE 754-2008, section 3.6, "interchange format" with k = 16):
+ *   1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ *   exponent field 0       : subnormal, value = frac * 2^-24
+ *   exponent field 1..30   : normal,    value = (1024 + frac) * 2^(e - 25)
+ *   exponent field 31      : infinity (frac == 0) or NaN.
+ * Every finite binary16 value is an integer multiple of 2^-24; in the binade
+ * [2^E, 2^(E+1)) with E >= -14 the spacing is 2^(E-10); below 2^-14 the
+ * spacing is 2^-24.  The largest finite value is 65504 = 2047 * 2^5.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* binary16 decode: the value a bit pattern stands for                 */
+/* ------------------------------------------------------------------ */
+static double f16_decode(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1F;
+    const int frac = h & 0x3FF;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);                 /* zero or subnormal */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);  /* normal */
+    }
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------------ */
+/* binary16 encode: round a double to the nearest binary16, ties even  */
+/* ------------------------------------------------------------------ */
+static uint16_t f16_encode(double x) {
+    uint64_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    const uint16_t sign = (uint16_t)((bits >> 48) & 0x8000u);
+    const int eb = (int)((bits >> 52) & 0x7FF);          /* biased double exponent */
+    const uint64_t man = bits & 0x000FFFFFFFFFFFFFull;
+
+    if (eb == 0x7FF) {                                    /* inf or NaN */
+        if (man == 0) return sign | 0x7C00u;
+        return sign | 0x7E00u;                            /* a quiet NaN */
+    }
+    if (eb == 0) return sign;                             /* |x| < 2^-1022 rounds to zero */
+
+    /* |x| = sig * 2^(eb - 1075), sig a 53-bit integer with its top bit set. */
+    const uint64_t sig = (1ull << 52) | man;
+    const int E = eb - 1023;                              /* floor(log2 |x|) */
+    if (E >= 16) return sign | 0x7C00u;                   /* >= 65536: overflow */
+
+    /* Spacing of binary16 values around |x| is 2^q. */
+    const int q = (E > -14 ? E : -14) - 10;
+    /* n = |x| / 2^q = sig * 2^(eb - 1075 - q); the shift is >= 42. */
+    const int s = q + 1075 - eb;
+    uint64_t n;
+    if (s >= 64) {
+        n = 0;                                            /* |x| < 2^-25 * 2^-10: far below half a step */
+    } else {
+        n = sig >> s;
+        const uint64_t rem = sig & ((1ull << s) - 1);
+        const uint64_t half = 1ull << (s - 1);
+        if (rem > half || (rem == half && (n & 1))) n += 1;   /* nearest, ties to even */
+    }
+    /* result = n * 2^q */
+    int qq = q;
+    if (qq == -24 && n < 1024) return sign | (uint16_t)n;   /* subnormal (or zero) */
+    if (n == 2048) { n = 1024; qq += 1; }                     /* rounded up into the next binade */
+    const int expo = qq + 10 + 15;                            /* biased binary16 exponent */
+    if (expo >= 31) return sign | 0x7C00u;                    /* overflow to infinity */
+    return sign | (uint16_t)(expo << 10) | (uint16_t)(n - 1024);
+}
+
+/* Decode table built from f16_decode, so the inner loop does not re-derive
+ * each value.  Built once, thread-safely. */
+static double g_decode[65536];
+static pthread_once_t g_decode_once = PTHREAD_ONCE_INIT;
+static void build_decode_table(void) {
+    for (uint32_t h = 0; h < 65536u; ++h) g_decode[h] = f16_decode((uint16_t)h);
+}
+static const double* decode_table(void) {
+    pthread_once(&g_decode_once, build_decode_table);
+    return g_decode;
+}
+
+/* One element of the definition: ascending k, one fp64 accumulator. */
+static double dot_row_row(const double* dec, const uint16_t* a_row, const uint16_t* b_row, int64_t K) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) acc += dec[a_row[k]] * dec[b_row[k]];
+    return acc;
+}
+
+/* ------------------------------------------------------------------ */
+/* exported: element conversions                                       */
+/* ------------------------------------------------------------------ */
+void oracle_f16_to_f64(const uint16_t* h, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f16_decode(h[i]);
+}
+
+void oracle_f64_to_f16(const double* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f16_encode(x[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* exported: GEMM over a list of (row, col) entries                    */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    const uint16_t* A;
+    const uint16_t* B;
+    int64_t M, N, K;
+    const int64_t* rows;   /* entries mode */
+    const int64_t* cols;
+    int64_t count;
+    int64_t row_begin;     /* rows mode */
+    int64_t row_end;
+    double* sums;          /* optional fp64 output */
+    uint16_t* out;         /* optional fp16 output */
+    int nthreads;
+    int tid;
+} job_t;
+
+static void* entries_worker(void* p) {
+    job_t* j = (job_t*)p;
+    const double* dec = decode_table();
+    for (int64_t i = j->tid; i < j->count; i += j->nthreads) {
+        const int64_t m = j->rows[i], n = j->cols[i];
+        const double acc = dot_row_row(dec, j->A + m * j->K, j->B + n * j->K, j->K);
+        if (j->sums) j->sums[i] = acc;
+        if (j->out) j->out[i] = f16_encode(acc);
+    }
+    return NULL;
+}
+
+static void* rows_worker(void* p) {
+    job_t* j = (job_t*)p;
+    const double* dec = decode_table();
+    /* thread tid takes one contiguous block of the (row, col) entries */
+    const int64_t total = (j->row_end - j->row_begin) * j->N;
+    const int64_t lo = total * j->tid / j->nthreads;
+    const int64_t hi = total * (j->tid + 1) / j->nthreads;
+    for (int64_t idx = lo; idx < hi; ++idx) {
+        const int64_t m = j->row_begin + idx / j->N;
+        const int64_t n = idx % j->N;
+        const double acc = dot_row_row(dec, j->A + m * j->K, j->B + n * j->K, j->K);
+        if (j->sums) j->sums[idx] = acc;
+        if (j->out) j->out[idx] = f16_encode(acc);
+    }
+    return NULL;
+}
+
+static int run_threads(job_t* proto, void* (*fn)(void*)) {
+    int nt = proto->nthreads < 1 ? 1 : proto->nthreads;
+    if (nt > 1024) nt = 1024;
+    proto->nthreads = nt;
+    job_t* jobs = (job_t*)malloc(sizeof(job_t) * (size_t)nt);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!jobs || !th) { free(jobs); free(th); return -1; }
+    int started = 0;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t] = *proto;
+        jobs[t].tid = t;
+        if (t == 0) continue;
+        if (pthread_create(&th[t], NULL, fn, &jobs[t]) != 0) break;
+        started = t;
+    }
+    /* thread 0's share runs here; shares of threads that failed to start
+     * are picked up serially so the result is always complete */
+    fn(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = started + 1; t < nt; ++t) fn(&jobs[t]);
+    free(jobs);
+    free(th);
+    return 0;
+}
+
+/* D entries at (rows[i], cols[i]); sums (fp64, unrounded) and/or out (fp16
+ * bits) may be NULL.  Returns 0, or -1 on bad arguments. */
+int oracle_gemm_nt_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                           const int64_t* rows, const int64_t* cols, int64_t count,
+                           double* sums, uint16_t* out, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+    for (int64_t i = 0; i < count; ++i)
+        if (rows[i] < 0 || rows[i] >= M || cols[i] < 0 || cols[i] >= N) return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.A = A; j.B = B; j.M = M; j.N = N; j.K = K;
+    j.rows = rows; j.cols = cols; j.count = count;
+    j.sums = sums; j.out = out; j.nthreads = nthreads;
+    return run_threads(&j, entries_worker);
+}
+
+/* Rows [row_begin, row_end) of D, all N columns, written row-major into
+ * out[(m - row_begin) * N + n] (and/or sums).  Returns 0, or -1. */
+int oracle_gemm_nt_rows(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                        int64_t row_begin, int64_t row_end,
+                        double* sums, uint16_t* out, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || row_begin < 0 || row_end > M || row_begin > row_end) return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.A = A; j.B = B; j.M = M; j.N = N; j.K = K;
+    j.row_begin = row_begin; j.row_end = row_end;
+    j.sums = sums; j.out = out; j.nthreads = nthreads;
+    return run_threads(&j, rows_worker);
+}
