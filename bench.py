@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the dense fp16 GEMM D = A·Bᵀ (fp16 in, fp32 accumulate, fp16 out).
+
+One step = one D = A·Bᵀ over the headline workload (M = N = K = 8192,
+entries normal(0, 1/√K), seeded) through the C ABI, with the operands
+already resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+--impl reference times the CPU oracle instead (the only other code that
+computes the same D), on this machine's host cores, on a bounded sample of
+the same workload (a block of output rows per step).
+
+Under torchrun with N > 1 ranks every rank runs its own replica of the
+workload on its own GPU (the GEMM has no exchange step); the value is the
+work of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dense_fp16_gemm_f16_gb300 import inputs, metrics  # noqa: E402
+
+METRIC = "fp16 GEMM TFLOPS (2MNK/t) at 8192³ on 1 GB300; % of dense-fp16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0      # used only if the measured-peaks file is absent
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ---------------------------------------------------------------- host-side helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def source_digest() -> str:
+    """sha256 over the CUDA sources: identifies the kernel the ncu counters were taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp16_gemm_f16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_sha256") != source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the benchmark runs."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []
+        self.window = None
+        self._stop = threading.Event()
+        self._proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               "-i", str(gpu_index), "-lms", str(period_ms)]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self._proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self._proc is None:
+            return None
+        time.sleep(0.15)
+        self._proc.terminate()
+        try:
+            self._proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self._proc.kill()
+        self._thread.join(timeout=5)
+        rows = self.samples
+        if self.window:
+            inside = [s for s in rows if self.window[0] <= s[0] <= self.window[1]]
+            rows = inside if inside else rows
+        if not rows:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for _, p in rows if num(p[0]) is not None]
+        smax = [num(p[1]) for _, p in rows if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in rows for i in range(4) if p[4 + i].lower() == "active"})
+        power = [num(p[2]) for _, p in rows if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None):
+    """Time the oracle on a block of output rows sized to take about target_s."""
+    import oracle
+    o = oracle.default()
+    threads = oracle.default_threads()
+    M, K = A.shape
+    N = B.shape[0]
+    t = time.perf_counter()
+    o.gemm_rows(A, B, 0, 1, nthreads=threads)
+    one = max(time.perf_counter() - t, 1e-4)
+    rows = int(max(1, min(M, target_s / one)))
+    if max_rows:
+        rows = min(rows, max_rows)
+    t = time.perf_counter()
+    o.gemm_rows(A, B, 0, rows, nthreads=threads)
+    dt = time.perf_counter() - t
+    return rows, dt, threads
+
+
+def cpu_baseline(A, B, target_s: float) -> dict:
+    M, K = A.shape
+    N = B.shape[0]
+    rows, dt, threads = oracle_rows_timing(A, B, target_s)
+    return {"value": metrics.tflops(rows, N, K, dt), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of D ({rows}x{N} outputs, K={K}) of the same seeded "
+                      f"operands, fp64 accumulation, {dt:.2f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    w = inputs.WORKLOADS[args.workload]
+    A, B = inputs.workload_operands(args.workload)
+    import oracle
+    o = oracle.default()
+    threads = oracle.default_threads()
+    # bound the whole run to a few minutes: size each step's sample of rows
+    budget = 120.0
+    per_step = max(0.05, min(2.0, budget / max(1, args.steps + args.warmup)))
+    t = time.perf_counter()
+    o.gemm_rows(A, B, 0, 1, nthreads=threads)
+    one = max(time.perf_counter() - t, 1e-4)
+    rows = int(max(1, min(w.M, per_step / one)))
+    for i in range(args.warmup):
+        r0 = (i * rows) % max(1, w.M - rows + 1)
+        o.gemm_rows(A, B, r0, r0 + rows, nthreads=threads)
+    times = []
+    for i in range(args.steps):
+        r0 = (i * rows) % max(1, w.M - rows + 1)
+        t = time.perf_counter()
+        o.gemm_rows(A, B, r0, r0 + rows, nthreads=threads)
+        times.append(time.perf_counter() - t)
+    sec = sum(times) / len(times)
+    value = metrics.tflops(rows, w.N, w.K, sec)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "sample_rows_per_step": rows, "note": "CPU oracle on a bounded sample of rows"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of D per step ({rows}x{w.N} outputs, K={w.K})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args):
+    import torch
+    import dense_fp16_gemm_f16_gb300 as g
+    from dense_fp16_gemm_f16_gb300 import build as gbuild
+
+    rank, local_rank, world = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    gbuild.build()
+    g.load()
+    w = inputs.WORKLOADS[args.workload]
+    A_h, B_h = inputs.workload_operands(args.workload)
+    stream = torch.cuda.Stream(device=dev)
+    A = torch.from_numpy(A_h).to(dev)
+    B = torch.from_numpy(B_h).to(dev)
+    D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    plan = g.gemm_f16_nt_plan(w.M, w.N, w.K)
+    lib = g.load()
+    s_handle = stream.cuda_stream
+    a_ptr, b_ptr, d_ptr = A.data_ptr(), B.data_ptr(), D.data_ptr()
+
+    def step():
+        st = lib.gemm_f16_nt(a_ptr, b_ptr, d_ptr, w.M, w.N, w.K, s_handle)
+        if st != 0:
+            raise g.GemmError(st, "gemm_f16_nt")
+
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    g.gemm_f16_nt_check(stream=stream, device=dev)
+
+    # timed region: K launches back to back on `stream`, an event pair around each
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if pg:
+        pg.barrier()
+    g.gemm_f16_nt_check(stream=stream, device=dev)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = starts[0].elapsed_time(ends[-1])
+    ms_per_step = region_ms / args.steps
+    if pg:
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    if sampler:
+        sampler.mark(t_wall0, t_wall1)
+
+    value = world * metrics.tflops(w.M, w.N, w.K, ms_per_step * 1e-3)
+    launch_ms = sum(per_launch_ms) / len(per_launch_ms)
+
+    # end to end through the C ABI: pinned host operands in, pinned host result out
+    e2e = None
+    if not args.no_e2e:
+        A_pin = torch.from_numpy(A_h).pin_memory()
+        B_pin = torch.from_numpy(B_h).pin_memory()
+        D_pin = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                A.copy_(A_pin, non_blocking=True)
+                B.copy_(B_pin, non_blocking=True)
+                step()
+                D_pin.copy_(D, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if pg:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        g.gemm_f16_nt_check(stream=stream, device=dev)
+        e2e = {"value": world * metrics.tflops(w.M, w.N, w.K, e2e_ms * 1e-3), "unit": UNIT,
+               "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": A_pin.numel() * 2 + B_pin.numel() * 2,
+               "d2h_bytes_per_step": D_pin.numel() * 2}
+
+    clocks = sampler.stop() if sampler else None
+    if pg:
+        pg.barrier()
+    if rank != 0:
+        pg.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        # dense fp16 and bf16 tensor rates are the same on this architecture (ratio 1)
+        peak = float(peaks["bf16_tflops"])
+        peak_src = "measured (bf16 cuBLAS burst, fp16 rate = bf16 rate)"
+    else:
+        peak = FALLBACK_PEAK_TFLOPS
+        peak_src = "fallback"
+    achieved = metrics.tflops(w.M, w.N, w.K, launch_ms * 1e-3)
+    if plan["variant"] == "SKINNY_SPLITK":
+        hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else 6800.0
+        gbs = metrics.gbs(w.compulsory_bytes, launch_ms * 1e-3)
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": recorded_traffic(w.name), "peak_source": "measured" if peaks else "fallback"}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name), "peak_source": peak_src}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(A_h, B_h, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "accumulate": "f32",
+                   "variant": plan["variant"], "grid_ctas": plan["grid_ctas"],
+                   "l2": "inputs larger than L2 (A+B = %d MiB > 129 MB); no flush" %
+                         ((w.M * w.K + w.N * w.K) * 2 >> 20) if (w.M * w.K + w.N * w.K) * 2 > 129e6
+                   else "inputs smaller than L2: warm-L2 number",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "per_launch_ms_min": min(per_launch_ms), "per_launch_ms_median": statistics.median(per_launch_ms)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,191 @@
-"""GB300-native dense fp16 GEMM D = A·Bᵀ (binding added with the C-ABI)."""
+"""GB300-native dense fp16 GEMM, D = A·Bᵀ (fp16 in, fp32 accumulate, fp16 out).
+
+This module is the Python binding of the C ABI declared in
+``include/gemm_f16.h``: the same entry-point names, argument marshalling only.
+Every step of the GEMM runs in the library's sm_103a kernels; there is no
+CPU or library fallback, and every call fails loudly (``GemmError`` /
+``LibraryMissing``) when the compiled library is absent or refuses the call.
+
+Tensors may be passed as CUDA ``torch.Tensor`` objects (float16, 2-D,
+row-major contiguous) or as raw device pointers (ints) with explicit sizes.
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libgemm_f16.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID_VALUE = 1
+    ERR_MISALIGNED = 2
+    ERR_UNSUPPORTED_DEVICE = 3
+    ERR_LAUNCH = 4
+    ERR_TIMEOUT = 5
+    ERR_CUDA = 6
+
+
+class Variant(enum.IntEnum):
+    AUTO = 0
+    TILE_2CTA_256x256 = 1
+    TILE_1CTA_128x128 = 2
+    TILE_1CTA_128x256 = 3
+    SKINNY_SPLITK = 4
+
+
+class LibraryMissing(RuntimeError):
+    """The compiled CUDA library is not there (build it first)."""
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{where}: {gemm_status_string(status)}")
+
+
+class Plan(ctypes.Structure):
+    """Mirror of gemm_plan_t."""
+    _fields_ = [
+        ("variant", ctypes.c_int32), ("cta_group", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+        ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+        ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
+        ("grid_ctas", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
+        ("max_tiles_per_cta", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["variant"] = Variant(d["variant"]).name
+        return d
+
+
+def load():
+    """Load libgemm_f16.so (once); raises LibraryMissing if it was never built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise LibraryMissing(
+                f"{LIB_PATH} is missing: build it with `python -m dense_fp16_gemm_f16_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.gemm_f16_nt.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.gemm_f16_nt.restype = ctypes.c_int
+        lib.gemm_f16_nt_variant.argtypes = [p, p, p, i64, i64, i64, ctypes.c_int, p]
+        lib.gemm_f16_nt_variant.restype = ctypes.c_int
+        lib.gemm_f16_nt_check.argtypes = [p]
+        lib.gemm_f16_nt_check.restype = ctypes.c_int
+        lib.gemm_status_string.argtypes = [ctypes.c_int]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_f16_nt_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(Plan)]
+        lib.gemm_f16_nt_plan.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def gemm_status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- marshalling
+def _is_tensor(x) -> bool:
+    return hasattr(x, "data_ptr") and hasattr(x, "dtype")
+
+
+def _stream_handle(stream, device=None) -> int | None:
+    if stream is None:
+        if device is not None:
+            import torch
+            return torch.cuda.current_stream(device).cuda_stream or None
+        return None
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _operands(A, B, D, M, N, K):
+    """(a_ptr, b_ptr, d_ptr, M, N, K, device) from tensors or raw pointers."""
+    if _is_tensor(A):
+        import torch
+        for name, t in (("A", A), ("B", B), ("D", D)):
+            if not _is_tensor(t):
+                raise TypeError(f"{name}: mix of tensors and raw pointers")
+            if t.dtype != torch.float16:
+                raise TypeError(f"{name} must be torch.float16, got {t.dtype}")
+            if not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if t.dim() != 2 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a 2-D row-major contiguous tensor")
+        if A.device != B.device or A.device != D.device:
+            raise ValueError("A, B and D must be on the same device")
+        m, k = A.shape
+        n, kb = B.shape
+        if kb != k or tuple(D.shape) != (m, n):
+            raise ValueError(f"shapes do not match D[M,N] = A[M,K]·B[N,K]ᵀ: {tuple(A.shape)}, "
+                             f"{tuple(B.shape)}, {tuple(D.shape)}")
+        for name, given, actual in (("M", M, m), ("N", N, n), ("K", K, k)):
+            if given is not None and given != actual:
+                raise ValueError(f"{name}={given} does not match the tensors ({actual})")
+        return A.data_ptr(), B.data_ptr(), D.data_ptr(), m, n, k, A.device
+    if M is None or N is None or K is None:
+        raise ValueError("raw pointers need explicit M, N and K")
+    return int(A or 0), int(B or 0), int(D or 0), int(M), int(N), int(K), None
+
+
+def _call(fn_name: str, args, device):
+    lib = load()
+    fn = getattr(lib, fn_name)
+    if device is not None:
+        import torch
+        with torch.cuda.device(device):
+            st = fn(*args)
+    else:
+        st = fn(*args)
+    if st != Status.OK:
+        raise GemmError(st, fn_name)
+
+
+def gemm_f16_nt(A, B, D, M=None, N=None, K=None, stream=None) -> None:
+    """D = A·Bᵀ on ``stream`` (default: the tensors' current stream); asynchronous."""
+    a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K)
+    _call("gemm_f16_nt", (a or None, b or None, d or None, m, n, k, _stream_handle(stream, dev)), dev)
+
+
+def gemm_f16_nt_variant(A, B, D, M=None, N=None, K=None, variant=Variant.AUTO, stream=None) -> None:
+    """gemm_f16_nt with an explicit kernel choice (a ``Variant``)."""
+    a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K)
+    _call("gemm_f16_nt_variant",
+          (a or None, b or None, d or None, m, n, k, int(variant), _stream_handle(stream, dev)), dev)
+
+
+def gemm_f16_nt_check(stream=None, device=None) -> None:
+    """Synchronise ``stream`` and raise GemmError if a kernel reported a timeout."""
+    handle = _stream_handle(stream, device)
+    _call("gemm_f16_nt_check", (handle,), device)
+
+
+def gemm_f16_nt_plan(M: int, N: int, K: int, variant=Variant.AUTO, num_sms: int = 0) -> dict:
+    """What a call would run (variant, tiles, grid, shared memory, workspace)."""
+    plan = Plan()
+    st = load().gemm_f16_nt_plan(int(M), int(N), int(K), int(variant), int(num_sms), ctypes.byref(plan))
+    if st != Status.OK:
+        raise GemmError(st, "gemm_f16_nt_plan")
+    return plan.as_dict()
+
+
+def gemm(A, B, variant=Variant.AUTO, stream=None):
+    """Convenience: allocate D with torch on A's device and return A·Bᵀ."""
+    import torch
+    D = torch.empty((A.shape[0], B.shape[0]), dtype=torch.float16, device=A.device)
+    gemm_f16_nt_variant(A, B, D, variant=variant, stream=stream)
+    return D

@@ -1,0 +1,450 @@
+// api.cu -- the C ABI declared in include/gemm_f16.h: argument validation,
+// the host-side planner, CUtensorMap encoding, per-stream workspaces and the
+// launch of the chosen kernel.  Every step of the GEMM itself runs in the
+// kernels; nothing here computes on the CPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "config.h"
+#include "gemm_f16.h"
+#include "launch.h"
+
+using namespace gemm_gb300;
+
+namespace {
+
+// Device status word: 0, or the first timeout any kernel recorded (see wait.cuh).
+__device__ uint32_t g_status_word;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    bool unsupported = false;
+    int sms = 0;
+    uint32_t* status = nullptr;
+    int max_clusters_2cta = 0;   // co-resident 2-CTA clusters of the 256x256 kernel
+    int per_sm_1cta128 = 0;      // co-resident CTAs per SM
+    int per_sm_1cta256 = 0;
+};
+
+struct Workspace {
+    float* partials = nullptr;
+    size_t partial_bytes = 0;
+    uint32_t* counters = nullptr;
+    size_t n_counters = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, void*>, Workspace> g_workspaces;
+EncodeTiledFn g_encode = nullptr;
+
+constexpr int64_t kMaxDim = INT32_MAX;
+constexpr int kGroupM = 8;
+
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
+// ----------------------------------------------------------------- planner
+struct Limits {
+    int sms;
+    int max_clusters_2cta;
+    int per_sm_1cta128;
+    int per_sm_1cta256;
+};
+
+int skinny_mn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant, const Limits& lim,
+                        gemm_plan_t* pl) {
+    std::memset(pl, 0, sizeof(*pl));
+    const gemm_status_t st = check_sizes(M, N, K);
+    if (st != GEMM_OK) return st;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
+    if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
+
+    if (variant == GEMM_VARIANT_AUTO) {
+        if (M <= 64) {
+            variant = GEMM_VARIANT_SKINNY_SPLITK;
+        } else {
+            // the pair kernel when its 256x256 tiles fill at least one wave of
+            // CTA pairs, else 128x128 tiles on single CTAs
+            const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
+            const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
+            variant = (t2 >= pairs) ? GEMM_VARIANT_TILE_2CTA_256x256 : GEMM_VARIANT_TILE_1CTA_128x128;
+        }
+    }
+    pl->variant = variant;
+    pl->tile_k = kBK;
+    pl->k_blocks = cdiv(K, kBK);
+
+    if (variant == GEMM_VARIANT_SKINNY_SPLITK) {
+        const int mn = skinny_mn(M);
+        const SkinnyOps& ops = skinny_ops(mn);
+        pl->cta_group = 1;
+        pl->tile_m = mn;
+        pl->tile_n = 128;
+        pl->stages = ops.stages;
+        pl->smem_bytes = ops.smem_bytes;
+        pl->tmem_cols = ops.tmem_cols;
+        pl->m_tiles = 1;
+        pl->n_tiles = cdiv(N, 128);
+        if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+        const int64_t units = pl->n_tiles * pl->k_blocks;
+        const int64_t G = units < lim.sms ? units : lim.sms;
+        int64_t max_t = 1;
+        for (int64_t c = 0; c < G; ++c) {
+            const int64_t u0 = unit_begin(c, units, G), u1 = unit_begin(c + 1, units, G);
+            const int64_t span = (u1 - 1) / pl->k_blocks - u0 / pl->k_blocks + 1;
+            if (span > max_t) max_t = span;
+        }
+        pl->grid_ctas = static_cast<int32_t>(G);
+        pl->max_tiles_per_cta = static_cast<int32_t>(max_t);
+        pl->workspace_bytes = round_up(G * max_t * mn * 128 * 4, 256) + round_up(pl->n_tiles * 4, 256);
+        return GEMM_OK;
+    }
+
+    const TiledOps& ops = variant == GEMM_VARIANT_TILE_2CTA_256x256 ? tiled_ops_2cta256()
+                          : variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
+                                                                      : tiled_ops_1cta256();
+    pl->cta_group = ops.cta_group;
+    pl->tile_m = ops.tile_m;
+    pl->tile_n = ops.tile_n;
+    pl->stages = ops.stages;
+    pl->smem_bytes = ops.smem_bytes;
+    pl->tmem_cols = ops.tmem_cols;
+    pl->m_tiles = cdiv(M, ops.tile_m);
+    pl->n_tiles = cdiv(N, ops.tile_n);
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    const int64_t tiles = pl->m_tiles * pl->n_tiles;
+    int64_t grid;
+    if (ops.cta_group == 2) {
+        const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
+        grid = 2 * (tiles < pairs ? tiles : pairs);
+    } else {
+        const int per_sm = variant == GEMM_VARIANT_TILE_1CTA_128x128 ? lim.per_sm_1cta128 : lim.per_sm_1cta256;
+        const int64_t slots = static_cast<int64_t>(lim.sms) * (per_sm > 0 ? per_sm : 1);
+        grid = tiles < slots ? tiles : slots;
+    }
+    if (grid <= 0) return GEMM_ERR_INVALID_VALUE;
+    pl->grid_ctas = static_cast<int32_t>(grid);
+    return GEMM_OK;
+}
+
+// ----------------------------------------------------------------- device set-up
+gemm_status_t get_device(DeviceState** out, int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_devices[dev];
+    if (d.unsupported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            d.unsupported = true;
+            return GEMM_ERR_UNSUPPORTED_DEVICE;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        void* status = nullptr;
+        if (cudaGetSymbolAddress(&status, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        const TiledOps* tiled[3] = {&tiled_ops_2cta256(), &tiled_ops_1cta128(), &tiled_ops_1cta256()};
+        for (const TiledOps* t : tiled)
+            if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+        for (int mn : {16, 32, 64})
+            if (skinny_ops(mn).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+        int clusters = 0, per128 = 0, per256 = 0;
+        if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
+            tiled[2]->max_active(&per256) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        d.sms = sms;
+        d.status = static_cast<uint32_t*>(status);
+        d.max_clusters_2cta = clusters;
+        d.per_sm_1cta128 = per128;
+        d.per_sm_1cta256 = per256;
+        d.ready = true;
+    }
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return GEMM_OK;
+}
+
+Limits limits_of(const DeviceState& d) {
+    return Limits{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256};
+}
+
+// 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// box of box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
+bool encode_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, uint32_t box_inner,
+               uint32_t box_outer) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                                strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+gemm_status_t get_workspace(int dev, gemm_stream_t stream, size_t partial_bytes, size_t n_counters,
+                            Workspace** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = g_workspaces[std::make_pair(dev, static_cast<void*>(stream))];
+    if (w.partial_bytes < partial_bytes) {
+        // growing: the old buffer may still be in use by work queued on this stream
+        if (w.partials) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+            cudaFree(w.partials);
+            w.partials = nullptr;
+            w.partial_bytes = 0;
+        }
+        if (cudaMalloc(&w.partials, partial_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            w.partials = nullptr;
+            return GEMM_ERR_CUDA;
+        }
+        w.partial_bytes = partial_bytes;
+    }
+    if (w.n_counters < n_counters) {
+        if (w.counters) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+            cudaFree(w.counters);
+            w.counters = nullptr;
+            w.n_counters = 0;
+        }
+        if (cudaMalloc(&w.counters, n_counters * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            w.counters = nullptr;
+            return GEMM_ERR_CUDA;
+        }
+        // counters start at zero; every call leaves them at zero again
+        if (cudaMemset(w.counters, 0, n_counters * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        w.n_counters = n_counters;
+    }
+    *out = &w;
+    return GEMM_OK;
+}
+
+bool ranges_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    if (a_bytes <= 0 || b_bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t timeout_for(int64_t k_blocks) {
+    // two seconds plus a generous 2 us per K block of the longest tile
+    return 2000000000ull + static_cast<uint64_t>(k_blocks) * 2000ull;
+}
+
+gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                  gemm_variant_t variant, gemm_stream_t stream) {
+    // ---- host-only argument checks (nothing touches a device before these pass)
+    gemm_status_t st = check_sizes(M, N, K);
+    if (st != GEMM_OK) return st;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+    const int64_t a_bytes = M * K * 2, b_bytes = N * K * 2, d_bytes = M * N * 2;
+    if (ranges_overlap(D, d_bytes, A, a_bytes) || ranges_overlap(D, d_bytes, B, b_bytes))
+        return GEMM_ERR_INVALID_VALUE;
+    if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_MISALIGNED;
+
+    DeviceState* dev = nullptr;
+    int dev_id = 0;
+    st = get_device(&dev, &dev_id);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (K == 0) {  // the empty sum
+        if (cudaMemsetAsync(D, 0, static_cast<size_t>(d_bytes), s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    }
+
+    gemm_plan_t pl;
+    st = make_plan(M, N, K, variant, limits_of(*dev), &pl);
+    if (st != GEMM_OK) return st;
+
+    if (pl.variant == GEMM_VARIANT_SKINNY_SPLITK) {
+        const SkinnyOps& ops = skinny_ops(pl.tile_m);
+        CUtensorMap tw, tx;
+        if (!encode_2d(&tw, B, K, N, kBK, 128) || !encode_2d(&tx, A, K, M, kBK, static_cast<uint32_t>(ops.mn)))
+            return GEMM_ERR_INVALID_VALUE;
+        Workspace* ws = nullptr;
+        const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
+        st = get_workspace(dev_id, stream, partial_bytes, static_cast<size_t>(pl.n_tiles), &ws);
+        if (st != GEMM_OK) return st;
+        SkinnyParams p;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.n_tiles = static_cast<int32_t>(pl.n_tiles);
+        p.k_blocks = static_cast<int32_t>(pl.k_blocks);
+        p.num_ctas = pl.grid_ctas;
+        p.max_tiles_per_cta = pl.max_tiles_per_cta;
+        p.units = pl.n_tiles * pl.k_blocks;
+        p.partials = ws->partials;
+        p.counters = ws->counters;
+        p.D = D;
+        p.status = dev->status;
+        p.timeout_ns = timeout_for(pl.k_blocks);
+        if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+
+    const TiledOps& ops = pl.variant == GEMM_VARIANT_TILE_2CTA_256x256 ? tiled_ops_2cta256()
+                          : pl.variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
+                                                                         : tiled_ops_1cta256();
+    CUtensorMap ta, tb, td;
+    if (!encode_2d(&ta, A, K, M, kBK, 128) ||
+        !encode_2d(&tb, B, K, N, kBK, static_cast<uint32_t>(ops.tile_n / ops.cta_group)) ||
+        !encode_2d(&td, D, N, M, 64, 32))
+        return GEMM_ERR_INVALID_VALUE;
+    TiledParams p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    p.m_tiles = pl.m_tiles;
+    p.n_tiles = pl.n_tiles;
+    p.num_tiles = pl.m_tiles * pl.n_tiles;
+    p.group_m = pl.m_tiles < kGroupM ? pl.m_tiles : kGroupM;
+    p.status = dev->status;
+    p.timeout_ns = timeout_for(pl.k_blocks);
+    if (ops.launch(ta, tb, td, p, pl.grid_ctas, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_API gemm_status_t gemm_f16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                                   gemm_stream_t stream) {
+    return run(A, B, D, M, N, K, GEMM_VARIANT_AUTO, stream);
+}
+
+GEMM_API gemm_status_t gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                           int64_t K, gemm_variant_t variant, gemm_stream_t stream) {
+    return run(A, B, D, M, N, K, variant, stream);
+}
+
+GEMM_API gemm_status_t gemm_f16_nt_check(gemm_stream_t stream) {
+    DeviceState* dev = nullptr;
+    int dev_id = 0;
+    gemm_status_t st = get_device(&dev, &dev_id);
+    if (st != GEMM_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (word == 0) return GEMM_OK;
+    // clear the word, and re-arm the skinny counters a cut-short kernel may have left set
+    cudaMemset(dev->status, 0, sizeof(uint32_t));
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (auto& kv : g_workspaces)
+            if (kv.first.first == dev_id && kv.second.counters)
+                cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(uint32_t));
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    const uint32_t code = word & 0xFFu;
+    return code == GEMM_ERR_TIMEOUT ? GEMM_ERR_TIMEOUT : GEMM_ERR_CUDA;
+}
+
+GEMM_API const char* gemm_status_string(gemm_status_t status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: bad size, pointer, overlap or variant";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: pointers must be 16-byte aligned, K and N multiples of 8";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel gave up waiting on a barrier";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
+    }
+    return "unknown gemm_status_t";
+}
+
+GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
+                                        int32_t num_sms, gemm_plan_t* plan) {
+    if (plan == nullptr) return GEMM_ERR_INVALID_VALUE;
+    Limits lim;
+    if (num_sms > 0) {
+        lim = Limits{num_sms, num_sms / 2, 1, 1};
+    } else {
+        DeviceState* dev = nullptr;
+        const gemm_status_t st = get_device(&dev, nullptr);
+        if (st != GEMM_OK) return st;
+        lim = limits_of(*dev);
+    }
+    return make_plan(M, N, K, variant, lim, plan);
+}
+
+}  // extern "C"

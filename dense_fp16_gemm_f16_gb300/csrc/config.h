@@ -1,0 +1,145 @@
+// config.h -- tile configurations and the index arithmetic that the host
+// planner and the kernels must agree on (grouped tile raster, the skinny
+// kernel's split of the K loop across CTAs).  Host and device code.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+#if defined(__CUDACC__)
+#define GEMM_HD __host__ __device__ __forceinline__
+#else
+#define GEMM_HD inline
+#endif
+
+namespace gemm_gb300 {
+
+// One pipeline stage covers 64 K elements: one 128-byte row of fp16, the
+// width of the 128-byte swizzle ("Building a Tiled GEMM", step 1: BLK_K = 64
+// with a 128-byte-swizzled SMEM layout).
+constexpr int kBK = 64;
+// Warp roles of every kernel: warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 2..5 are the epilogue warpgroup (warp w reads TMEM
+// lanes 32*(w%4) .. 32*(w%4)+31).
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
+
+GEMM_HD int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ tiled
+// Persistent, warp-specialised kernel.  CG = CTAs per MMA (1, or 2 for a
+// cta_group::2 pair in a 2-CTA cluster), BN = output columns per tile.  A tile
+// is BM = 128*CG rows by BN columns; each CTA of a pair loads its own 128 rows
+// of A and its own BN/CG rows of B and owns 128 accumulator rows in its TMEM.
+template <int CG_, int BN_, int STAGES_>
+struct TiledConfig {
+    static constexpr int CG = CG_;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 128 * CG;
+    static constexpr int A_ROWS = 128;
+    static constexpr int B_ROWS = BN / CG;
+    static constexpr int A_BYTES = A_ROWS * kBK * 2;
+    static constexpr int B_BYTES = B_ROWS * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
+    static constexpr int TMEM_COLS = 2 * BN;                 // two accumulator buffers
+    static constexpr int EPI_COLS = 64;                      // columns per TMA store box
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // one warp's 32 rows
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 2 * EPI_BUF_BYTES;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;  // + slack to align the base
+    static constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 up to 256");
+    static_assert(B_ROWS <= 256, "TMA box rows are limited to 256");
+    static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
+    static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+};
+
+using Cfg2cta256 = TiledConfig<2, 256, 6>;
+using Cfg1cta128 = TiledConfig<1, 128, 6>;
+using Cfg1cta256 = TiledConfig<1, 256, 4>;
+
+struct TiledParams {
+    int32_t M, N, K;
+    int32_t k_blocks;
+    int64_t m_tiles, n_tiles;
+    int64_t num_tiles;
+    int64_t group_m;          // tile rows per raster group
+    uint32_t* status;         // device status word (0 = ok)
+    uint64_t timeout_ns;      // per-wait budget
+};
+
+// Grouped raster: tiles are numbered in groups of `group_m` tile rows; inside
+// a group the tile row varies fastest, so CTAs working at the same time share
+// A rows and B rows through L2.
+GEMM_HD void tile_coords(int64_t t, int64_t m_tiles, int64_t n_tiles, int64_t group_m,
+                         int64_t& tm, int64_t& tn) {
+    const int64_t per_group = group_m * n_tiles;
+    const int64_t g = t / per_group;
+    const int64_t first_m = g * group_m;
+    const int64_t rows = (m_tiles - first_m < group_m) ? (m_tiles - first_m) : group_m;
+    const int64_t r = t - g * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+// ------------------------------------------------------------------ skinny
+// Small-M kernel: D^T = B * A^T computed with the operands' roles swapped, so
+// the 128-row MMA side runs over N (the weight rows) and the narrow MMA N
+// side (MN = 16, 32 or 64) over M.  The (n-tile, k-block) units are split
+// into G contiguous ranges, one per CTA; tiles cut across ranges are summed
+// in a fixed order by the last CTA to finish one of their pieces.
+template <int MN_, int STAGES_>
+struct SkinnyConfig {
+    static constexpr int MN = MN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int W_BYTES = 128 * kBK * 2;   // weight (B) tile: 128 rows
+    static constexpr int X_BYTES = MN * kBK * 2;    // activation (A) tile: MN rows
+    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    static constexpr int TMEM_COLS = (2 * MN < 32) ? 32 : 2 * MN;
+    static constexpr int OFF_W = 0;
+    static constexpr int OFF_X = OFF_W + STAGES * W_BYTES;
+    static constexpr int OFF_BAR = OFF_X + STAGES * X_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
+    static constexpr uint32_t IDESC = ptx::idesc_f16_f32(128, MN);
+    static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
+    static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
+    static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
+};
+
+using CfgSkinny16 = SkinnyConfig<16, 8>;
+using CfgSkinny32 = SkinnyConfig<32, 8>;
+using CfgSkinny64 = SkinnyConfig<64, 8>;
+
+struct SkinnyParams {
+    int32_t M, N, K;
+    int32_t n_tiles, k_blocks;
+    int32_t num_ctas;         // G
+    int32_t max_tiles_per_cta;
+    int64_t units;            // n_tiles * k_blocks
+    float* partials;          // [G][max_tiles_per_cta][MN][128] fp32
+    uint32_t* counters;       // [n_tiles], zero between calls
+    void* D;                  // __half [M][N]
+    uint32_t* status;
+    uint64_t timeout_ns;
+};
+
+// First unit of CTA c's range; CTA c owns [unit_begin(c), unit_begin(c+1)).
+GEMM_HD int64_t unit_begin(int64_t c, int64_t units, int64_t G) { return c * units / G; }
+
+// The CTA whose range holds unit u.
+GEMM_HD int64_t cta_of_unit(int64_t u, int64_t units, int64_t G) {
+    return ((u + 1) * G - 1) / units;
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,232 @@
+// kernel_skinny.cuh -- small-M GEMM (M <= 64): D^T = B * A^T with split K.
+//
+// With M this small a 128-row MMA over M would be mostly padding and the
+// run time is set by reading B (the N x K weights) once from HBM -- the
+// "small batch leaves memory bandwidth unused" situation of the GEMM blog
+// post (section 5.4).  So the operands swap roles: each MMA is
+// tcgen05.mma M=128 (128 rows of B, i.e. 128 output columns) x N=MN (the M
+// rows of A, padded to 16/32/64 by TMA zero fill) x K=16, both operands
+// K-major exactly as stored.  The accumulator tile in TMEM is D^T: TMEM lane
+// = output column n, TMEM column = output row m.
+//
+// Work split: the (n-tile, k-block) units are laid out tile-major and cut into
+// G contiguous ranges, one per CTA (G = number of SMs), so every SM streams
+// the same number of B bytes.  A tile whose K loop lies inside one CTA's range
+// is written straight to D.  A tile cut across CTAs gets one fp32 partial per
+// CTA in a workspace; the CTA that finishes last (per-tile counter) adds the
+// partials in ascending CTA order -- a fixed order, so results are bitwise
+// reproducible -- converts to fp16, writes D and re-arms the counter.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "config.h"
+#include "ptx.cuh"
+#include "wait.cuh"
+
+namespace gemm_gb300 {
+
+template <int MN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[MN]) {
+    if constexpr (MN == 16) {
+        ptx::tmem_ld_x16(taddr, v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < MN / 32; ++i) ptx::tmem_ld_x32(taddr + 32 * i, v + 32 * i);
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const SkinnyParams p) {
+    constexpr int MN = Cfg::MN;
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+    const uint32_t sbase = ptx::smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t slot = sbase + Cfg::OFF_SLOT;
+    volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT + 4);
+
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmW);
+        ptx::prefetch_tensormap(&tmX);
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<1>(slot, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish<1>();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT);
+
+    const int64_t G = p.num_ctas;
+    const int64_t W = p.units;
+    const int64_t KB = p.k_blocks;
+    const int64_t c = blockIdx.x;
+    const int64_t u0 = unit_begin(c, W, G);
+    const int64_t u1 = unit_begin(c + 1, W, G);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int64_t t = u / KB;
+                const int32_t kx = static_cast<int32_t>((u - t * KB) * kBK);
+                if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                ptx::tma_load_2d(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES, &tmW, full_bar(stage), kx,
+                                 static_cast<int32_t>(t * 128));
+                ptx::tma_load_2d(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES, &tmX, full_bar(stage), kx, 0);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            for (int i = 0; ok && i < STAGES; ++i) {
+                ok = wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t seg = 0;
+            for (int64_t u = u0; ok && u < u1; ++seg) {
+                const int64_t t = u / KB;
+                const int64_t seg_end = (t + 1) * KB < u1 ? (t + 1) * KB : u1;
+                const uint32_t buf = seg & 1u;
+                const uint32_t use = (seg >> 1) & 1u;
+                if (!wait_phase(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * MN;
+                for (const int64_t seg_start = u; u < seg_end; ++u) {
+                    if (!wait_phase(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t w_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES);
+                    const uint64_t x_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, Cfg::IDESC,
+                                        (u != seg_start || k != 0) ? 1u : 0u);
+                    ptx::mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull_bar(buf));
+            }
+            ptx::mma_commit(drain_bar);
+            wait_phase(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r = q * 32 + lane;                     // row of the 128-row tile = output column
+        const int etid = threadIdx.x - 64;               // 0..127 among the epilogue threads
+        __half* D = static_cast<__half*>(p.D);
+        const int64_t first_tile = u0 / KB;
+        uint32_t seg = 0;
+        for (int64_t u = u0; u < u1; ++seg) {
+            const int64_t t = u / KB;
+            const int64_t seg_end = (t + 1) * KB < u1 ? (t + 1) * KB : u1;
+            const uint32_t buf = seg & 1u;
+            const uint32_t use = (seg >> 1) & 1u;
+            // all four epilogue warps take the same decision: they meet at
+            // named barriers below
+            const bool ready = wait_phase(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
+            if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) break;
+            ptx::tc_fence_after();
+            uint32_t v[MN];
+            tmem_ld_cols<MN>(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * MN, v);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+
+            const int64_t n = t * 128 + r;
+            const int64_t c_first = cta_of_unit(t * KB, W, G);
+            const int64_t c_last = cta_of_unit(t * KB + KB - 1, W, G);
+            if (c_first == c_last) {
+                // the whole K loop of this tile ran here
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MN; ++m)
+                        if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(__uint_as_float(v[m]));
+                }
+            } else {
+                float* mine = p.partials +
+                              ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
+#pragma unroll
+                for (int m = 0; m < MN; ++m) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
+                __threadfence();
+                ptx::named_bar_sync(1, 32 * kEpiWarps);
+                if (etid == 0) {
+                    const uint32_t prev = atomicAdd(p.counters + t, 1u);
+                    *last_flag = (prev == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+                }
+                ptx::named_bar_sync(1, 32 * kEpiWarps);
+                if (*last_flag) {
+                    __threadfence();
+                    if (n < p.N) {
+                        for (int m = 0; m < MN && m < p.M; ++m) {
+                            float acc = 0.0f;
+                            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                                const int64_t j = t - unit_begin(cc, W, G) / KB;
+                                acc += __ldcg(p.partials + ((cc * p.max_tiles_per_cta + j) * MN + m) * 128 + r);
+                            }
+                            D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(acc);
+                        }
+                    }
+                    if (etid == 0) p.counters[t] = 0u;  // re-armed for the next call on this stream
+                }
+                ptx::named_bar_sync(1, 32 * kEpiWarps);  // last_flag is reused by the next segment
+            }
+            u = seg_end;
+        }
+    }
+
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,255 @@
+// kernel_tiled.cuh -- persistent, warp-specialised tcgen05 GEMM D = A * B^T.
+//
+// The data path is the Blackwell one of "Building a Tiled GEMM" (MLC),
+// sections "GEMM data path" and steps 1-3: operand tiles GMEM -> SMEM
+// (128-byte swizzle, 64-wide K chunks), tcgen05.mma into a TMEM fp32
+// accumulator that stays in place across the K loop (step 2), one output tile
+// per unit of work (step 3).  Past those steps it applies the chapter's
+// optimisation roadmap ("Optimisation roadmap"): TMA loads tracked by
+// mbarriers, a multi-stage SMEM ring so loads overlap MMAs, a persistent tile
+// loop, warp specialisation (producer / MMA / writeback), and, for CG == 2, a
+// CTA pair that computes one larger MMA tile together.
+//
+// Roles (kThreads = 192):
+//   warp 0, one lane   TMA producer: for every tile and K block, wait for a
+//                      free stage, then load this CTA's A rows and B rows.
+//   warp 1             allocates / frees TMEM; in the leader CTA one lane
+//                      issues the MMAs (only one thread issues, as step 1 of
+//                      the chapter requires) and commits them to barriers.
+//   warps 2-5          epilogue: TMEM -> registers -> fp16 -> swizzled SMEM
+//                      -> TMA store, clipped at the edges of D.
+// The accumulator is double-buffered in TMEM, so the epilogue of one tile
+// runs while the MMAs of the next tile are issued.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "config.h"
+#include "ptx.cuh"
+#include "wait.cuh"
+
+namespace gemm_gb300 {
+
+template <class Cfg>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmD, const TiledParams p) {
+    constexpr int CG = Cfg::CG;
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    // Align the working area to 1024 bytes (the 128-byte swizzle atom); every
+    // CTA of a pair gets the same offsets, which the pair MMA relies on.
+    const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+    const uint32_t sbase = ptx::smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+
+    const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t slot = sbase + Cfg::OFF_SLOT;
+
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmD);
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival + TMA bytes
+            ptx::mbar_init(empty_bar(s), 1);  // one MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);                 // one MMA commit
+            ptx::mbar_init(tempty_bar(b), kEpiWarps * CG);   // every epilogue warp of the pair
+        }
+        ptx::mbar_init(drain_bar, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(slot, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
+    }
+    ptx::tc_fence_before();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT);
+
+    const int64_t cluster_idx = blockIdx.x / CG;
+    const int64_t num_clusters = gridDim.x / CG;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t t = cluster_idx; ok && t < p.num_tiles; t += num_clusters) {
+                int64_t tm, tn;
+                tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+                const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * Cfg::A_ROWS);
+                const int32_t b_row = static_cast<int32_t>(tn * Cfg::BN + rank * Cfg::B_ROWS);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
+                                    p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_dst = sbase + Cfg::OFF_A + stage * Cfg::A_BYTES;
+                    const uint32_t b_dst = sbase + Cfg::OFF_B + stage * Cfg::B_BYTES;
+                    if constexpr (CG == 1) {
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                        ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, a_row);
+                        ptx::tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, b_row);
+                    } else {
+                        // Both CTAs' bytes complete on the leader's full barrier; the
+                        // leader announces the pair's total.
+                        const uint32_t leader_full = ptx::mapa(full_bar(stage), 0);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+                        ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
+                        ptx::tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Do not leave while an MMA commit may still arrive on this CTA's
+            // barriers: wait until the MMA has released every stage.
+            for (int i = 0; ok && i < STAGES; ++i) {
+                ok = wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (rank == 0 && lane == 0) {
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;
+            for (int64_t t = cluster_idx; ok && t < p.num_tiles; t += num_clusters, ++it) {
+                const uint32_t buf = it & 1u;
+                const uint32_t use = (it >> 1) & 1u;
+                // the epilogue must have drained this accumulator buffer
+                if (!wait_phase(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * Cfg::BN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_A + stage * Cfg::A_BYTES);
+                    const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_B + stage * Cfg::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // +32 bytes (2 in the >>4 address field) per 16-wide K step;
+                        // the first product of a tile overwrites the accumulator.
+                        ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                                         (kb | k) != 0 ? 1u : 0u);
+                    }
+                    // release the stage to the producers once these MMAs have read it
+                    if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
+                    else ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                // accumulator of this tile complete: hand it to the epilogues
+                if constexpr (CG == 1) ptx::mma_commit(tfull_bar(buf));
+                else ptx::mma_commit_pair(tfull_bar(buf), 0x3);
+            }
+            // every MMA this thread issued has finished before TMEM is freed
+            if constexpr (CG == 1) ptx::mma_commit(drain_bar);
+            else ptx::mma_commit_pair(drain_bar, 0x1);
+            wait_phase(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;    // TMEM lanes 32q .. 32q+31 are readable by this warp
+        const int ew = warp - 2;   // owner of staging buffers 2ew, 2ew+1
+        const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(tempty_bar(0), 0) : tempty_bar(0);
+        uint32_t it = 0;
+        int ebuf = 0;
+        for (int64_t t = cluster_idx; t < p.num_tiles; t += num_clusters, ++it) {
+            int64_t tm, tn;
+            tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+            const uint32_t buf = it & 1u;
+            const uint32_t use = (it >> 1) & 1u;
+            if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns))
+                break;
+            ptx::tc_fence_after();
+            const int64_t row0 = tm * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
+            const bool rows_in = row0 < p.M;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
+#pragma unroll 1
+            for (int c = 0; c < Cfg::BN / Cfg::EPI_COLS; ++c) {
+                uint32_t v[64];
+                ptx::tmem_ld_x32(t_row + c * 64, v);
+                ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
+                ptx::tmem_wait_ld();
+                if (c == Cfg::BN / Cfg::EPI_COLS - 1) {
+                    // this warp has read its part of the buffer: return it to the MMA
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2) ptx::mbar_arrive_cluster(tempty_leader0 + 8u * buf);
+                        else ptx::mbar_arrive(tempty_bar(buf));
+                    }
+                }
+                const int64_t col0 = tn * Cfg::BN + c * Cfg::EPI_COLS;
+                const bool store = rows_in && col0 < p.N;  // warp-uniform
+                // the TMA store issued two chunks ago from this buffer has read it
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t* sb = smem + Cfg::OFF_EPI + (ew * 2 + ebuf) * Cfg::EPI_BUF_BYTES;
+                if (store) {
+                    // row `lane` of the box, 16-byte chunk j at position j ^ (row % 8):
+                    // the layout the 128-byte-swizzled tensor map expects
+                    uint8_t* row_ptr = sb + lane * (Cfg::EPI_COLS * 2);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t h[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 x = __floats2half2_rn(__uint_as_float(v[8 * j + 2 * e]),
+                                                                __uint_as_float(v[8 * j + 2 * e + 1]));
+                            h[e] = *reinterpret_cast<const uint32_t*>(&x);
+                        }
+                        *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(h[0], h[1], h[2], h[3]);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (store)
+                        ptx::tma_store_2d(&tmD, ptx::smem_u32(sb), static_cast<int32_t>(col0),
+                                          static_cast<int32_t>(row0));
+                    ptx::bulk_commit_group();
+                }
+                ebuf ^= 1;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncwarp();
+    ptx::tc_fence_before();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,35 @@
+// launch.h -- host-side entry points into each compiled kernel variant.  Each
+// variant lives in its own translation unit; the C-ABI layer (api.cu) only
+// sees these function tables.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "config.h"
+
+namespace gemm_gb300 {
+
+struct TiledOps {
+    int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols;
+    // set the kernel's shared-memory limit on the current device
+    cudaError_t (*prepare)();
+    // co-resident clusters (cta_group 2) or CTAs per SM (cta_group 1) on the current device
+    cudaError_t (*max_active)(int* out);
+    cudaError_t (*launch)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                          const TiledParams& p, int grid_ctas, cudaStream_t stream);
+};
+
+struct SkinnyOps {
+    int mn, stages, smem_bytes, tmem_cols;
+    cudaError_t (*prepare)();
+    cudaError_t (*launch)(const CUtensorMap& w, const CUtensorMap& x, const SkinnyParams& p,
+                          int grid_ctas, cudaStream_t stream);
+};
+
+const TiledOps& tiled_ops_2cta256();
+const TiledOps& tiled_ops_1cta128();
+const TiledOps& tiled_ops_1cta256();
+const SkinnyOps& skinny_ops(int mn);  // mn = 16, 32 or 64
+
+}  // namespace gemm_gb300

@@ -1,0 +1,63 @@
+// launch_tiled.cuh -- builds the TiledOps table of one tiled configuration.
+#pragma once
+
+#include "kernel_tiled.cuh"
+#include "launch.h"
+
+namespace gemm_gb300 {
+
+template <class Cfg>
+struct TiledLauncher {
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::SMEM_BYTES);
+    }
+
+    static cudaError_t max_active(int* out) {
+        if constexpr (Cfg::CG == 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg>, &cfg);
+        } else {
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg>, kThreads,
+                                                                 Cfg::SMEM_BYTES);
+        }
+    }
+
+    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                              const TiledParams& p, int grid_ctas, cudaStream_t stream) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        cfg.numAttrs = 0;
+        if constexpr (Cfg::CG == 2) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.numAttrs = 1;
+        }
+        cfg.attrs = attr;
+        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg>, a, b, d, p);
+    }
+
+    static const TiledOps& ops() {
+        static const TiledOps o = {Cfg::CG, Cfg::BM, Cfg::BN, Cfg::STAGES, Cfg::SMEM_BYTES,
+                                   Cfg::TMEM_COLS, &prepare, &max_active, &launch};
+        return o;
+    }
+};
+
+}  // namespace gemm_gb300

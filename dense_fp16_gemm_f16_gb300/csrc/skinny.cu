@@ -1,0 +1,39 @@
+// The small-M split-K kernels (narrow MMA side of 16, 32 or 64 rows).
+#include "kernel_skinny.cuh"
+#include "launch.h"
+
+namespace gemm_gb300 {
+namespace {
+
+template <class Cfg>
+struct SkinnyLauncher {
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(gemm_skinny_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::SMEM_BYTES);
+    }
+    static cudaError_t launch(const CUtensorMap& w, const CUtensorMap& x, const SkinnyParams& p,
+                              int grid_ctas, cudaStream_t stream) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.numAttrs = 0;
+        cfg.attrs = nullptr;
+        return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<Cfg>, w, x, p);
+    }
+    static const SkinnyOps& ops() {
+        static const SkinnyOps o = {Cfg::MN, Cfg::STAGES, Cfg::SMEM_BYTES, Cfg::TMEM_COLS, &prepare, &launch};
+        return o;
+    }
+};
+
+}  // namespace
+
+const SkinnyOps& skinny_ops(int mn) {
+    if (mn <= 16) return SkinnyLauncher<CfgSkinny16>::ops();
+    if (mn <= 32) return SkinnyLauncher<CfgSkinny32>::ops();
+    return SkinnyLauncher<CfgSkinny64>::ops();
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,150 @@
+/*
+ * gemm_f16.h -- C ABI of the GB300 (sm_103a) dense fp16 GEMM library.
+ *
+ * The operation ("Building a Tiled GEMM", MLC Modern GPU Programming for
+ * MLSys, section "GEMM"):
+ *
+ *     D[m,n] = sum_{k<K} A[m,k] * B[n,k]        i.e.  D = A * B^T
+ *
+ * A is M x K and B is N x K, both row-major fp16 (IEEE binary16).  B is the
+ * linear-layer weight layout and is read as stored: it is never transposed
+ * or repacked.  Products accumulate in fp32 (same section: fp16 storage, fp32
+ * accumulator); D is written as fp16, converted from the fp32 sum with
+ * round-to-nearest-even.  The throughput figure the library is measured by
+ * is TFLOPS = 2*M*N*K / (t * 1e12) (same section, and the headline table of
+ * the Croqtile tutorial "dense GEMM fp16 from naive").
+ *
+ * Conventions for every entry point below:
+ *   - A, B and D are DEVICE pointers (cudaMalloc memory or a CUDA tensor's
+ *     storage) owned by the caller; the library never frees or keeps them.
+ *   - Rows are dense: the leading dimension of A and B is K elements, of D
+ *     it is N elements.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream):
+ *     they validate their arguments on the host, enqueue the kernel(s) and
+ *     return.  A returned GEMM_OK means "enqueued"; device-side failures are
+ *     reported by gemm_f16_nt_check().
+ *   - Argument errors are returned synchronously and nothing is enqueued.
+ *   - The library uses the CUDA device that is current on the calling thread.
+ *
+ * Scratch memory.  The skinny (small-M, split-K) kernel keeps fp32 partial
+ * sums and per-tile counters in a workspace the library allocates with
+ * cudaMalloc on the first call that needs it for a given (device, stream)
+ * pair, grows when a larger problem needs more, and keeps until the process
+ * exits.  Calls on the same stream are ordered and share that workspace
+ * safely; calls on different streams get different workspaces.
+ */
+#ifndef GEMM_F16_H_
+#define GEMM_F16_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL means the legacy default stream. */
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* negative or > INT32_MAX size, NULL pointer with a
+                                        non-empty problem, D overlapping A or B, or a variant
+                                        that cannot run this shape */
+    GEMM_ERR_MISALIGNED = 2,         /* a pointer not 16-byte aligned, or K or N not a
+                                        multiple of 8 (TMA needs 16-byte row pitches) */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* the current device is not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = 4,             /* the kernel launch itself failed */
+    GEMM_ERR_TIMEOUT = 5,            /* a kernel gave up waiting on one of its barriers
+                                        (reported by gemm_f16_nt_check) */
+    GEMM_ERR_CUDA = 6                /* another CUDA runtime call failed (no device,
+                                        out of memory for the workspace, ...) */
+} gemm_status_t;
+
+/* Kernel choices.  GEMM_VARIANT_AUTO picks one from the shape. */
+typedef enum {
+    GEMM_VARIANT_AUTO = 0,
+    GEMM_VARIANT_TILE_2CTA_256x256 = 1, /* persistent, 2-CTA cluster, 256x256 tile per pair */
+    GEMM_VARIANT_TILE_1CTA_128x128 = 2, /* persistent, one CTA per 128x128 tile */
+    GEMM_VARIANT_TILE_1CTA_128x256 = 3, /* persistent, one CTA per 128x256 tile */
+    GEMM_VARIANT_SKINNY_SPLITK = 4      /* M <= 64: operands swapped, K split across all SMs */
+} gemm_variant_t;
+
+/*
+ * gemm_f16_nt -- D = A * B^T, the operation above.
+ *
+ *   A  const __half[M][K], row-major, device memory, 16-byte aligned
+ *   B  const __half[N][K], row-major, device memory, 16-byte aligned
+ *   D  __half[M][N], row-major, device memory, 16-byte aligned; every element
+ *      is overwritten, nothing outside it is written; must not overlap A or B
+ *   M, N, K  sizes, 0 <= each <= INT32_MAX; K and N multiples of 8
+ *   stream   the stream the work is ordered on
+ *
+ * M == 0 or N == 0 is a no-op (GEMM_OK).  K == 0 writes D = 0 (the empty sum).
+ * The kernel path is hand-written sm_103a code (TMA, tcgen05.mma with a TMEM
+ * accumulator); there is no CPU or library fallback.
+ */
+GEMM_API gemm_status_t gemm_f16_nt(const void* A, const void* B, void* D,
+                          int64_t M, int64_t N, int64_t K, gemm_stream_t stream);
+
+/*
+ * gemm_f16_nt_variant -- gemm_f16_nt with the kernel chosen by the caller.
+ * Same arguments and semantics; `variant` selects the kernel.  Returns
+ * GEMM_ERR_INVALID_VALUE when the variant cannot run the shape (the skinny
+ * variant needs M <= 64).  All variants compute the same D up to the order
+ * of fp32 additions.
+ */
+GEMM_API gemm_status_t gemm_f16_nt_variant(const void* A, const void* B, void* D,
+                                  int64_t M, int64_t N, int64_t K,
+                                  gemm_variant_t variant, gemm_stream_t stream);
+
+/*
+ * gemm_f16_nt_check -- synchronise `stream`, then report and clear the
+ * device-side status word of the current device.  Returns GEMM_OK,
+ * GEMM_ERR_TIMEOUT if any kernel since the last check gave up waiting on a
+ * barrier (its output is then incomplete), or GEMM_ERR_CUDA if the stream
+ * reported an error.  After a timeout the skinny-kernel workspaces of the
+ * device are reset.
+ */
+GEMM_API gemm_status_t gemm_f16_nt_check(gemm_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+GEMM_API const char* gemm_status_string(gemm_status_t status);
+
+/* What a call would run, as decided by the host-side planner. */
+typedef struct {
+    int32_t variant;         /* the gemm_variant_t that runs (never AUTO) */
+    int32_t cta_group;       /* CTAs per MMA (1 or 2) */
+    int32_t tile_m;          /* output rows per tile (per CTA pair when cta_group == 2) */
+    int32_t tile_n;          /* output columns per tile */
+    int32_t tile_k;          /* K elements per pipeline stage */
+    int32_t stages;          /* shared-memory pipeline depth */
+    int64_t m_tiles, n_tiles;/* tile grid (skinny: m_tiles = 1, n_tiles = N tiles of 128) */
+    int64_t k_blocks;        /* ceil(K / tile_k) */
+    int32_t grid_ctas;       /* CTAs launched */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t tmem_cols;       /* TMEM columns allocated per CTA */
+    int32_t max_tiles_per_cta; /* skinny: partial-sum slots per CTA, else 0 */
+    int64_t workspace_bytes; /* skinny: fp32 partials + counters, else 0 */
+} gemm_plan_t;
+
+/*
+ * gemm_f16_nt_plan -- fill *plan with what gemm_f16_nt_variant(...variant...)
+ * would run for an M x N x K problem on a GPU with `num_sms` SMs.  Pure host
+ * code: it touches no device when num_sms > 0 (pass num_sms <= 0 to query the
+ * current device).  Returns the same argument errors as the GEMM call would
+ * for these sizes (pointers are not checked), or GEMM_OK.
+ */
+GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
+                               int32_t num_sms, gemm_plan_t* plan);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* GEMM_F16_H_ */

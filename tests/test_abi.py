@@ -1,0 +1,159 @@
+"""The C-ABI boundary on the host (no GPU): the library loads, exports every
+entry point its header declares, rejects bad arguments before touching a
+device, and plans the launch the way the pages' tiling arithmetic says."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp16_gemm_f16_gb300 as g
+from dense_fp16_gemm_f16_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+FAKE = 0x7F0000000000  # a 16-byte-aligned address that is never dereferenced here
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return g.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"GEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = _declared_functions()
+    assert "gemm_f16_nt" in names and len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_only_declared_symbols_are_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gbuild.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    exported = sorted(line.split()[-1] for line in out.stdout.splitlines() if line.strip())
+    assert exported == _declared_functions()
+
+
+def test_status_strings(lib):
+    for s in g.Status:
+        text = g.gemm_status_string(s)
+        assert text.startswith("GEMM_") or s == g.Status.OK
+    assert "unknown" in g.gemm_status_string(99)
+
+
+def _call(M, N, K, A=FAKE, B=FAKE + (1 << 32), D=FAKE + (2 << 32), variant=0):
+    lib = g.load()
+    return lib.gemm_f16_nt_variant(A, B, D, M, N, K, variant, None)
+
+
+def test_argument_errors_are_returned_before_any_device_call(lib):
+    S = g.Status
+    assert _call(-1, 8, 8) == S.ERR_INVALID_VALUE
+    assert _call(8, -8, 8) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, -8) == S.ERR_INVALID_VALUE
+    assert _call(2 ** 31, 8, 8) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, 8, variant=7) == S.ERR_INVALID_VALUE
+    assert _call(65, 8, 8, variant=g.Variant.SKINNY_SPLITK) == S.ERR_INVALID_VALUE
+    # empty problems are a no-op even with NULL pointers
+    assert _call(0, 8, 8, A=0, B=0, D=0) == S.OK
+    assert _call(8, 0, 8, A=0, B=0, D=0) == S.OK
+    # NULL pointers with work to do
+    assert _call(8, 8, 8, D=0) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, 8, A=0) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, 8, B=0) == S.ERR_INVALID_VALUE
+    # TMA needs 16-byte row pitches and 16-byte aligned bases
+    assert _call(8, 8, 12) == S.ERR_MISALIGNED
+    assert _call(8, 12, 8) == S.ERR_MISALIGNED
+    assert _call(8, 8, 8, A=FAKE + 2) == S.ERR_MISALIGNED
+    assert _call(8, 8, 8, D=FAKE + (2 << 32) + 8) == S.ERR_MISALIGNED
+    # D overlapping an operand
+    assert _call(64, 64, 64, D=FAKE + 64) == S.ERR_INVALID_VALUE
+    assert _call(64, 64, 64, B=FAKE + (2 << 32) + 8192 - 16) == S.ERR_INVALID_VALUE
+    # adjacent but not overlapping is fine for validation; on a machine with no
+    # GPU the call then fails at the first CUDA call, with a CUDA status
+    st = _call(64, 64, 64, A=FAKE, B=FAKE + 64 * 64 * 2, D=FAKE + 2 * 64 * 64 * 2)
+    assert st in (S.ERR_CUDA, S.ERR_UNSUPPORTED_DEVICE, S.OK)
+
+
+def test_python_binding_rejects_bad_arguments(lib):
+    with pytest.raises(ValueError):
+        g.gemm_f16_nt(FAKE, FAKE, FAKE)          # raw pointers without sizes
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(FAKE, FAKE + 2, FAKE + (2 << 32), 8, 8, 8)
+    assert e.value.status == g.Status.ERR_MISALIGNED
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [[int(v) for v in line.split()] for line in f if line.strip() and not line.startswith("#")]
+
+
+def test_tile_grid_matches_the_pages_examples(lib):
+    for M, N, K, mt, nt, tiles in _rows("tile_grid_examples.txt"):
+        p = g.gemm_f16_nt_plan(M, N, K, g.Variant.TILE_1CTA_128x128, num_sms=152)
+        assert (p["m_tiles"], p["n_tiles"], p["m_tiles"] * p["n_tiles"]) == (mt, nt, tiles)
+        assert p["tile_m"] == 128 and p["tile_n"] == 128 and p["tile_k"] == 64
+
+
+def test_plans_for_the_named_workloads(lib):
+    P = lambda *a, **k: g.gemm_f16_nt_plan(*a, num_sms=152, **k)  # noqa: E731
+    p = P(8192, 8192, 8192)
+    assert p["variant"] == "TILE_2CTA_256x256" and p["cta_group"] == 2
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 32, 128)
+    assert p["grid_ctas"] == 152 and p["tmem_cols"] == 512
+    p = P(4000, 11000, 4104)
+    assert p["variant"] == "TILE_2CTA_256x256"
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)   # ragged in M, N and K
+    p = P(1024, 1024, 2048)
+    assert p["variant"] == "TILE_1CTA_128x128" and p["grid_ctas"] == 64
+    p = P(128, 128, 64)
+    assert p["variant"] == "TILE_1CTA_128x128" and p["grid_ctas"] == 1 and p["k_blocks"] == 1
+    p = P(16, 8192, 8192)
+    assert p["variant"] == "SKINNY_SPLITK" and p["tile_m"] == 16 and p["n_tiles"] == 64
+    assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 2
+    assert p["workspace_bytes"] >= 152 * 2 * 16 * 128 * 4 + 64 * 4
+    for v in g.Variant:
+        if v in (g.Variant.AUTO,):
+            continue
+        q = P(64, 256, 128, variant=v)
+        assert q["variant"] == v.name
+        assert q["smem_bytes"] <= 232448
+
+
+def test_skinny_split_covers_every_unit_once(lib):
+    # tiny problems: fewer (tile, k-block) units than SMs -> one unit per CTA
+    p = g.gemm_f16_nt_plan(5, 8, 8, num_sms=152)
+    assert p["variant"] == "SKINNY_SPLITK" and p["grid_ctas"] == 1 and p["tile_m"] == 16
+    p = g.gemm_f16_nt_plan(33, 1024, 640, num_sms=152)
+    assert p["tile_m"] == 64 and p["grid_ctas"] == 8 * 10
+    # many tiles with short K: each CTA owns several whole tiles
+    p = g.gemm_f16_nt_plan(16, 65536, 64, num_sms=152)
+    assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 4   # 512 whole tiles over 152 CTAs
+
+
+def test_plan_errors(lib):
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_nt_plan(-1, 8, 8, num_sms=152)
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_nt_plan(100, 8, 8, variant=g.Variant.SKINNY_SPLITK, num_sms=152)
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_nt_plan(8, 8, 9, num_sms=152)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g, "LIB_PATH", "/nonexistent/libgemm_f16.so")
+    with pytest.raises(g.LibraryMissing):
+        g.load()

@@ -1,0 +1,224 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI (needs a GB300).
+
+Every comparison is element by element on the same seeded inputs: the full
+output at sizes the oracle finishes in seconds (several tiles, ragged
+tails), and at the full sizes of the named workloads -- in the launch
+configuration the benchmark times (the AUTO plan) -- all of 8 seeded rows,
+8 seeded columns, 65,536 seeded random entries, the corners, and the last
+row/column of every partial tile.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import dense_fp16_gemm_f16_gb300 as g
+from dense_fp16_gemm_f16_gb300 import build as gbuild
+from dense_fp16_gemm_f16_gb300 import inputs
+from gemm_check import check_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    gbuild.build()
+    g.load()
+    yield
+    g.gemm_f16_nt_check(device=torch.device("cuda"))
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _run(A, B, variant=g.Variant.AUTO, fill=float("nan"), stream=None):
+    """D = A·Bᵀ on the GPU through the C ABI; D is pre-filled with `fill`."""
+    dA, dB = _dev(A), _dev(B)
+    D = torch.full((A.shape[0], B.shape[0]), fill, dtype=torch.float16, device="cuda")
+    g.gemm_f16_nt_variant(dA, dB, D, variant=variant, stream=stream)
+    g.gemm_f16_nt_check(stream=stream, device=D.device)
+    return D.cpu().numpy()
+
+
+def _full_parity(A, B, variant=g.Variant.AUTO, what=""):
+    d = _run(A, B, variant)
+    ref = oracle.gemm(A, B)
+    return check_close(d, ref, A.shape[1], what or f"{variant.name} {A.shape[0]}x{B.shape[0]}x{A.shape[1]}")
+
+
+def _edge_indices(M, tile):
+    """Last index of every tile and first of the next, plus the last index."""
+    idx = set()
+    for t in range(tile, M + tile, tile):
+        for v in (t - 1, t, t - tile // 2 - 1, t - tile // 2):
+            if 0 <= v < M:
+                idx.add(v)
+    idx.add(M - 1)
+    return sorted(idx)
+
+
+# ---------------------------------------------------------------- named workloads
+SMALL = ["single_tile_128x128x64", "multi_tile_1024x1024x2048"]
+LARGE = ["square_8192x8192x8192", "ragged_4000x11000x4104", "skinny_16x8192x8192"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_named_workload_full_output(name):
+    A, B = inputs.workload_operands(name)
+    stats = _full_parity(A, B, what=name)
+    assert stats["rel_fro"] < 1e-3
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_named_workload_sampled(name):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.workload_operands(name)
+    plan = g.gemm_f16_nt_plan(w.M, w.N, w.K)
+    d = _run(A, B)
+    rows, cols = inputs.sample_entries(
+        w.M, w.N, seed=w.seed + 77,
+        extra_rows=_edge_indices(w.M, plan["tile_m"]) if plan["variant"] != "SKINNY_SPLITK" else range(w.M),
+        extra_cols=_edge_indices(w.N, plan["tile_n"]))
+    ref = oracle.gemm_entries(A, B, rows, cols)
+    check_close(d[rows, cols], ref, w.K, name)
+    assert not np.any(np.isnan(d)), f"{name}: unwritten output entries"
+
+
+# ---------------------------------------------------------------- every variant, ragged
+TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256]
+RAGGED = [(1, 8, 8), (7, 24, 40), (128, 128, 64), (129, 136, 72), (255, 264, 200),
+          (300, 520, 1000), (513, 256, 4104), (640, 1000, 520)]
+SKINNY = [(1, 8, 8), (5, 136, 64), (16, 128, 64), (17, 200, 72), (33, 1000, 520),
+          (64, 4096, 1024), (16, 1024, 8192), (3, 65536, 64)]
+
+
+@pytest.mark.parametrize("variant", TILED, ids=lambda v: v.name)
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+def test_tiled_variants_ragged(variant, shape):
+    M, N, K = shape
+    A, B = inputs.operands(M, N, K, seed=1000 + M + N + K)
+    _full_parity(A, B, variant)
+
+
+@pytest.mark.parametrize("shape", SKINNY, ids=lambda s: "x".join(map(str, s)))
+def test_skinny_variant_ragged(shape):
+    M, N, K = shape
+    A, B = inputs.operands(M, N, K, "normal:1", "normal:1/sqrtK", seed=2000 + M + N + K)
+    _full_parity(A, B, g.Variant.SKINNY_SPLITK)
+
+
+@pytest.mark.parametrize("shape", [(96, 512, 2048), (200, 300, 4104)], ids=str)
+def test_all_variants_agree(shape):
+    M, N, K = shape
+    A, B = inputs.operands(M, N, K, seed=31)
+    ref = oracle.gemm(A, B)
+    for v in TILED:
+        check_close(_run(A, B, v), ref, K, v.name)
+
+
+# ---------------------------------------------------------------- closed forms (exact)
+@pytest.mark.parametrize("variant", TILED + [g.Variant.SKINNY_SPLITK], ids=lambda v: v.name)
+def test_closed_forms_exact(variant):
+    M = 48 if variant == g.Variant.SKINNY_SPLITK else 272
+    # all ones: D = K exactly (fp32 holds every partial sum exactly)
+    for K in (64, 4104):
+        d = _run(np.ones((M, K), np.float16), np.ones((264, K), np.float16), variant)
+        assert np.all(d == K), (variant.name, K)
+    # identity B: D = A bit for bit
+    K = 256
+    A = inputs.draw(M, K, "uniform", seed=5)
+    d = _run(A, np.eye(K, dtype=np.float16), variant)
+    assert np.array_equal(d.view(np.uint16), A.view(np.uint16))
+    # swapping the operands transposes D
+    B = inputs.draw(136, K, "uniform", seed=6)
+    if variant == g.Variant.SKINNY_SPLITK:
+        return
+    d1 = _run(A, B, variant)
+    d2 = _run(B, A, variant)
+    check_close(d2, d1.T, K, "transpose")
+
+
+def test_special_values_propagate():
+    A = np.ones((130, 64), np.float16)
+    B = np.ones((136, 64), np.float16)
+    A[3, 5] = np.nan
+    A[7] = 256.0
+    B[9] = 256.0
+    d = _run(A, B, g.Variant.TILE_1CTA_128x128)
+    assert np.all(np.isnan(d[3]))
+    assert np.all(np.isposinf(d[7, 9:10]))       # 256*256*64 overflows fp16
+    assert d[8, 8] == 64 and d[7, 8] == 256 * 64
+
+
+# ---------------------------------------------------------------- determinism, streams
+@pytest.mark.parametrize("name_or_shape", ["multi_tile_1024x1024x2048", (16, 1024, 8192), (40, 5000, 3000)],
+                         ids=str)
+def test_bitwise_deterministic(name_or_shape):
+    if isinstance(name_or_shape, str):
+        A, B = inputs.workload_operands(name_or_shape)
+    else:
+        A, B = inputs.operands(*name_or_shape, seed=77)
+    d1 = _run(A, B)
+    d2 = _run(A, B)
+    assert np.array_equal(d1.view(np.uint16), d2.view(np.uint16))
+
+
+def test_skinny_split_tiles_rearm_between_calls():
+    # every tile's K loop is split over many CTAs: the fixed-order reduction
+    # and the counter reset are exercised on consecutive calls
+    for seed in (1, 2, 3):
+        A, B = inputs.operands(16, 1024, 8192, "normal:1", "normal:1/sqrtK", seed=seed)
+        _full_parity(A, B, g.Variant.SKINNY_SPLITK, what=f"skinny split seed {seed}")
+
+
+def test_side_stream():
+    A, B = inputs.operands(300, 640, 512, seed=8)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d = _run(A, B, stream=s)
+    check_close(d, oracle.gemm(A, B), 512, "side stream")
+    A, B = inputs.operands(16, 640, 4096, seed=9)
+    with torch.cuda.stream(s):
+        d = _run(A, B, stream=s)
+    check_close(d, oracle.gemm(A, B), 4096, "side stream skinny")
+
+
+# ---------------------------------------------------------------- edges of the contract
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    D = torch.full((40, 24), float("nan"), dtype=torch.float16, device="cuda")
+    A = torch.empty((40, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((24, 0), dtype=torch.float16, device="cuda")
+    g.gemm_f16_nt(A, B, D)
+    g.gemm_f16_nt_check(device=D.device)
+    assert torch.all(D == 0)
+    D0 = torch.full((0, 24), 1.0, dtype=torch.float16, device="cuda")
+    g.gemm_f16_nt(torch.empty((0, 8), dtype=torch.float16, device="cuda"),
+                  torch.ones((24, 8), dtype=torch.float16, device="cuda"), D0)
+
+
+def test_device_argument_errors():
+    buf = torch.zeros(1 << 20, dtype=torch.float16, device="cuda")
+    base = buf.data_ptr()
+    lib = g.load()
+    # misaligned A (2 bytes past a 16-byte boundary)
+    st = lib.gemm_f16_nt(base + 2, base + 65536, base + 131072, 64, 64, 64, None)
+    assert st == g.Status.ERR_MISALIGNED
+    # D aliasing B
+    st = lib.gemm_f16_nt(base, base + 65536, base + 65536 + 4096, 64, 64, 64, None)
+    assert st == g.Status.ERR_INVALID_VALUE
+    # nothing was launched, so the device is clean
+    g.gemm_f16_nt_check(device=buf.device)
+
+
+def test_plan_on_device_matches_sm_count():
+    p = g.gemm_f16_nt_plan(8192, 8192, 8192)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p["variant"] == "TILE_2CTA_256x256"
+    assert 2 <= p["grid_ctas"] <= sms and p["grid_ctas"] % 2 == 0
+    q = g.gemm_f16_nt_plan(16, 8192, 8192)
+    assert q["grid_ctas"] == sms
