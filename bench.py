@@ -46,10 +46,12 @@ CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="time an M x N x K problem (normal(0, 1/sqrt(K)) entries) instead of a named workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -188,12 +190,23 @@ def cpu_baseline(A, B, target_s: float) -> dict:
                       f"operands, fp64 accumulation, {dt:.2f} s"}
 
 
+def workload_of(args):
+    if args.shape:
+        M, N, K = args.shape
+        return inputs.Workload(f"shape_{M}x{N}x{K}", M, N, K, "normal:1/sqrtK", "normal:1/sqrtK", 99)
+    return inputs.WORKLOADS[args.workload]
+
+
+def operands_of(w):
+    return inputs.operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    w = inputs.WORKLOADS[args.workload]
-    A, B = inputs.workload_operands(args.workload)
+    w = workload_of(args)
+    A, B = operands_of(w)
     import oracle
     o = oracle.default()
     threads = oracle.default_threads()
@@ -248,8 +261,8 @@ def run_ours(args):
 
     gbuild.build()
     g.load()
-    w = inputs.WORKLOADS[args.workload]
-    A_h, B_h = inputs.workload_operands(args.workload)
+    w = workload_of(args)
+    A_h, B_h = operands_of(w)
     stream = torch.cuda.Stream(device=dev)
     A = torch.from_numpy(A_h).to(dev)
     B = torch.from_numpy(B_h).to(dev)
