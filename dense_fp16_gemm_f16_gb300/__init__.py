@@ -89,6 +89,8 @@ def load():
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_f16_nt_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(Plan)]
         lib.gemm_f16_nt_plan.restype = ctypes.c_int
+        lib.gemm_f16_nt_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.gemm_f16_nt_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -166,6 +168,19 @@ def gemm_f16_nt_variant(A, B, D, M=None, N=None, K=None, variant=Variant.AUTO, s
     a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K)
     _call("gemm_f16_nt_variant",
           (a or None, b or None, d or None, m, n, k, int(variant), _stream_handle(stream, dev)), dev)
+
+
+def gemm_f16_nt_noalloc(A, B, D, M=None, N=None, K=None, stream=None) -> None:
+    """Small-M (M <= 64) D = A·Bᵀ using only the library's fixed scratch array.
+
+    For callers that cannot let the library call cudaMalloc (a memory pool owns
+    the device, or an allocation's implicit synchronisation is not allowed at
+    this point).  Calls whose GPU work overlaps share that one array and race:
+    keep them ordered on one stream.  Make the first call on a device before
+    any stream capture (it looks up the array's device address).
+    """
+    a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K)
+    _call("gemm_f16_nt_noalloc", (a or None, b or None, d or None, m, n, k, _stream_handle(stream, dev)), dev)
 
 
 def gemm_f16_nt_check(stream=None, device=None) -> None:

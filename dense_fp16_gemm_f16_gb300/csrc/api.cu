@@ -374,6 +374,102 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     return GEMM_OK;
 }
 
+// ----------------------------------------------------------------- no-allocation entry
+// Scratch for gemm_f16_nt_noalloc: one fixed array per device that loads this
+// library, laid out as [per-tile counters, 256-byte padded][fp32 partials].
+// It exists from module load until the process exits; nothing here ever calls
+// cudaMalloc or cudaFree for it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[GEMM_F16_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 64;
+uint8_t* g_noalloc_ptr[kNoAllocMaxDevices] = {};  // device address of the array, per device
+
+// Set-up, once per device, with that device current: the array's name in host
+// code is only a host-side stand-in, so fetch its device address.
+gemm_status_t noalloc_scratch(int dev, uint8_t** out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_OK;
+}
+
+gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                          gemm_stream_t stream) {
+    gemm_status_t st = check_sizes(M, N, K);
+    if (st != GEMM_OK) return st;
+    if (M > 64) return GEMM_ERR_INVALID_VALUE;  // only the small-M kernel uses scratch
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+    const int64_t a_bytes = M * K * 2, b_bytes = N * K * 2, d_bytes = M * N * 2;
+    if (ranges_overlap(D, d_bytes, A, a_bytes) || ranges_overlap(D, d_bytes, B, b_bytes))
+        return GEMM_ERR_INVALID_VALUE;
+    if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_MISALIGNED;
+
+    DeviceState* dev = nullptr;
+    int dev_id = 0;
+    st = get_device(&dev, &dev_id);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        if (cudaMemsetAsync(D, 0, static_cast<size_t>(d_bytes), s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    }
+
+    gemm_plan_t pl;
+    st = make_plan(M, N, K, GEMM_VARIANT_SKINNY_SPLITK, limits_of(*dev), &pl);
+    if (st != GEMM_OK) return st;
+    const SkinnyOps& ops = skinny_ops(pl.tile_m);
+    const size_t counter_bytes = static_cast<size_t>(round_up(pl.n_tiles * 4, 256));
+    const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
+    if (counter_bytes + partial_bytes > static_cast<size_t>(GEMM_F16_NOALLOC_SCRATCH_BYTES))
+        return GEMM_ERR_INVALID_VALUE;  // larger than the fixed scratch: nothing is launched
+
+    uint8_t* scratch = nullptr;
+    st = noalloc_scratch(dev_id, &scratch);
+    if (st != GEMM_OK) return st;
+    CUtensorMap tw, tx;
+    if (!encode_2d(&tw, B, K, N, kBK, 128) || !encode_2d(&tx, A, K, M, kBK, static_cast<uint32_t>(ops.mn)))
+        return GEMM_ERR_INVALID_VALUE;
+    // The counters must start at zero.  Every completed call leaves them at
+    // zero, but the array is shared by all calls, so clear them on the stream
+    // rather than trust what an earlier (possibly cut-short) call left.
+    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    SkinnyParams p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.n_tiles = static_cast<int32_t>(pl.n_tiles);
+    p.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    p.num_ctas = pl.grid_ctas;
+    p.max_tiles_per_cta = pl.max_tiles_per_cta;
+    p.units = pl.n_tiles * pl.k_blocks;
+    p.partials = reinterpret_cast<float*>(scratch + counter_bytes);
+    p.counters = reinterpret_cast<uint32_t*>(scratch);
+    p.D = D;
+    p.status = dev->status;
+    p.timeout_ns = timeout_for(pl.k_blocks);
+    if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -445,6 +541,11 @@ GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_va
         lim = limits_of(*dev);
     }
     return make_plan(M, N, K, variant, lim, plan);
+}
+
+GEMM_API gemm_status_t gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                           int64_t K, gemm_stream_t stream) {
+    return run_noalloc(A, B, D, M, N, K, stream);
 }
 
 }  // extern "C"

@@ -143,6 +143,44 @@ typedef struct {
 GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
                                int32_t num_sms, gemm_plan_t* plan);
 
+/*
+ * gemm_f16_nt_noalloc -- the small-M GEMM (M <= 64) without any device
+ * allocation by the library.  (The pages have no counterpart: this entry
+ * point exists for callers of this library, not for the method.)
+ *
+ * Who it is for: callers that cannot call cudaMalloc -- a framework or
+ * serving engine that has handed (nearly) all device memory to its own pool,
+ * or code that must not risk the device-wide synchronisation a cudaMalloc or
+ * cudaFree can cause in the middle of a latency-critical sequence.
+ * gemm_f16_nt's small-M path needs a workspace of fp32 partial sums and
+ * per-tile counters that it allocates on first use; this entry point instead
+ * uses one fixed array compiled into the library (GEMM_F16_NOALLOC_SCRATCH_BYTES,
+ * 16 MiB), which every GPU that loads the library holds until the process exits.
+ *
+ * Arguments, layout, ownership and semantics are those of gemm_f16_nt; the
+ * caller still passes A, B and D (device memory).  It runs the same split-K
+ * kernel as GEMM_VARIANT_SKINNY_SPLITK and gives the same D.
+ *
+ * Errors: those of gemm_f16_nt, plus GEMM_ERR_INVALID_VALUE when M > 64 or when
+ * the problem needs more scratch than the fixed array holds (nothing is then
+ * enqueued).  Every M <= 64 with N <= 16384 fits, at any K; larger N fits for
+ * smaller M (the check is exact: 256-byte-padded counters of 4 bytes per
+ * 128 columns, plus 4 * 128 * MN bytes of partials per (CTA, tile) slot).
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and the library's per-device
+ * kernel settings; make that first call before any stream capture.
+ *
+ * Sharing: every call on every stream uses the same array, and it keeps the
+ * last call's contents.  Each call clears the counters it needs on `stream`
+ * before its kernel runs.  Calls whose work overlaps on the GPU (e.g. issued
+ * on two streams without ordering between them) race on the array and give
+ * wrong results: order them on one stream or with events.
+ */
+#define GEMM_F16_NOALLOC_SCRATCH_BYTES (16u << 20)
+GEMM_API gemm_status_t gemm_f16_nt_noalloc(const void* A, const void* B, void* D,
+                                  int64_t M, int64_t N, int64_t K, gemm_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
