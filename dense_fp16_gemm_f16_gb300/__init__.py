@@ -60,6 +60,7 @@ class Plan(ctypes.Structure):
         ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
         ("grid_ctas", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
         ("max_tiles_per_cta", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("num_full_tiles", ctypes.c_int64), ("tail_split", ctypes.c_int32), ("group_m", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

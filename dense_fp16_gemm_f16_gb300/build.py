@@ -59,25 +59,34 @@ def _run(cmd: list[str], verbose: bool) -> None:
         print(r.stdout, flush=True)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile the CUDA sources and link libgemm_f16.so; returns its path."""
-    if not force and not ptxas_info and not is_stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          extra_flags=(), lib_path: str | None = None) -> str:
+    """Compile the CUDA sources and link libgemm_f16.so; returns its path.
+
+    ``extra_flags`` (e.g. ``["-DGEMM_GROUP_M=16"]``) and ``lib_path`` build a
+    separately named copy with other compile-time settings; such builds always
+    recompile and never replace the default library.
+    """
+    custom = bool(extra_flags) or lib_path is not None
+    out = lib_path or LIB_PATH
+    if not force and not ptxas_info and not custom and not is_stale():
+        return out
+    build_dir = BUILD_DIR if not custom else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(extra_flags)
     objs = []
     cmds = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmds.append([cc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj])
     with cf.ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         list(ex.map(lambda c: _run(c, verbose or ptxas_info), cmds))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     _run([cc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs, "-Xlinker", "--exclude-libs,ALL"], verbose)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -51,7 +51,20 @@ std::map<std::pair<int, void*>, Workspace> g_workspaces;
 EncodeTiledFn g_encode = nullptr;
 
 constexpr int64_t kMaxDim = INT32_MAX;
-constexpr int kGroupM = 8;
+// Raster groups hold as many tile rows as keep the group's A rows (tile rows x
+// BM x K fp16) within this many bytes, so they stay in L2 while the group's
+// B blocks stream past (measured best: 8 tile rows at K = 8192, all 16 at
+// 4000 x 11000 x 4104).  GEMM_GROUP_M fixes the group size instead.
+constexpr int64_t kL2GroupBytes = 34ll << 20;
+
+int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K) {
+#ifdef GEMM_GROUP_M
+    const int64_t g = GEMM_GROUP_M;
+#else
+    const int64_t g = kL2GroupBytes / (static_cast<int64_t>(tile_m) * K * 2);
+#endif
+    return g < 1 ? 1 : (g > m_tiles ? m_tiles : g);
+}
 
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
@@ -136,17 +149,24 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     pl->n_tiles = cdiv(N, ops.tile_n);
     if (M == 0 || N == 0 || K == 0) return GEMM_OK;
     const int64_t tiles = pl->m_tiles * pl->n_tiles;
-    int64_t grid;
+    // slots = CTA pairs (or CTAs) that can be resident at once
+    int64_t slots;
     if (ops.cta_group == 2) {
-        const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
-        grid = 2 * (tiles < pairs ? tiles : pairs);
+        slots = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
     } else {
         const int per_sm = variant == GEMM_VARIANT_TILE_1CTA_128x128 ? lim.per_sm_1cta128 : lim.per_sm_1cta256;
-        const int64_t slots = static_cast<int64_t>(lim.sms) * (per_sm > 0 ? per_sm : 1);
-        grid = tiles < slots ? tiles : slots;
+        slots = static_cast<int64_t>(lim.sms) * (per_sm > 0 ? per_sm : 1);
     }
-    if (grid <= 0) return GEMM_ERR_INVALID_VALUE;
-    pl->grid_ctas = static_cast<int32_t>(grid);
+    if (slots <= 0) return GEMM_ERR_INVALID_VALUE;
+    int64_t num_full;
+    int split;
+    tail_split(tiles, slots, ops.tile_n, ops.cta_group, num_full, split);
+    const int64_t units = num_full + (tiles - num_full) * split;
+    const int64_t clusters = units < slots ? units : slots;
+    pl->grid_ctas = static_cast<int32_t>(clusters * ops.cta_group);
+    pl->num_full_tiles = num_full;
+    pl->tail_split = split;
+    pl->group_m = static_cast<int32_t>(raster_group(pl->m_tiles, ops.tile_m, K));
     return GEMM_OK;
 }
 
@@ -364,7 +384,11 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.m_tiles = pl.m_tiles;
     p.n_tiles = pl.n_tiles;
     p.num_tiles = pl.m_tiles * pl.n_tiles;
-    p.group_m = pl.m_tiles < kGroupM ? pl.m_tiles : kGroupM;
+    p.group_m = pl.group_m;
+    p.num_full = pl.num_full_tiles;
+    p.split = pl.tail_split;
+    p.reserved = 0;
+    p.num_units = pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
     if (ops.launch(ta, tb, td, p, pl.grid_ctas, s) != cudaSuccess) {

@@ -73,6 +73,10 @@ struct TiledParams {
     int64_t m_tiles, n_tiles;
     int64_t num_tiles;
     int64_t group_m;          // tile rows per raster group
+    int64_t num_full;         // tiles run whole: the persistent grid's full rounds
+    int64_t num_units;        // num_full + (num_tiles - num_full) * split
+    int32_t split;            // the remaining tiles are cut into `split` column pieces
+    int32_t reserved;
     uint32_t* status;         // device status word (0 = ok)
     uint64_t timeout_ns;      // per-wait budget
 };
@@ -91,19 +95,64 @@ GEMM_HD void tile_coords(int64_t t, int64_t m_tiles, int64_t n_tiles, int64_t gr
     tn = r / rows;
 }
 
+// Work unit u of the persistent loop -> (tile row tm, first column n0,
+// column count nw).  The first num_full units are whole tiles in raster
+// order; the tiles of the last, partly filled round are cut into `split`
+// column pieces so that more CTA pairs share that round.
+GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int64_t& n0, int& nw) {
+    int64_t t = u, piece = 0;
+    int s = 1;
+    if (u >= p.num_full) {
+        const int64_t v = u - p.num_full;
+        s = p.split;
+        t = p.num_full + v / s;
+        piece = v - (v / s) * s;
+    }
+    int64_t tn;
+    tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+    nw = BN / s;
+    n0 = tn * BN + piece * nw;
+}
+
+// Split of the last round: whole rounds of `slots` tiles run first; the
+// remaining tiles are cut into s column pieces (s = 1, 2 or 4, pieces at
+// least 64 columns wide).  A piece does 1/s of the MMA work, but each CTA
+// still loads all its 128 rows of A per K block, so its time is modelled as
+// max(1/s, (128 + BN/(CG*s)) / (128 + BN/CG)) of a whole tile; the tail costs
+// ceil(rem * s / slots) such piece times, and the cheapest s wins (ties keep
+// the smaller s).
+inline void tail_split(int64_t num_tiles, int64_t slots, int BN, int CG, int64_t& num_full, int& split) {
+    num_full = (num_tiles / slots) * slots;
+    const int64_t rem = num_tiles - num_full;
+    split = 1;
+    if (rem == 0) return;
+    double best = static_cast<double>(cdiv(rem, slots));
+    for (int s = 2; s <= 4 && BN / s >= 64; s *= 2) {
+        const double load = (128.0 + static_cast<double>(BN) / (CG * s)) / (128.0 + static_cast<double>(BN) / CG);
+        const double piece = load > 1.0 / s ? load : 1.0 / s;
+        const double cost = static_cast<double>(cdiv(rem * s, slots)) * piece;
+        if (cost < best - 1e-9) {
+            best = cost;
+            split = s;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ skinny
 // Small-M kernel: D^T = B * A^T computed with the operands' roles swapped, so
 // the 128-row MMA side runs over N (the weight rows) and the narrow MMA N
 // side (MN = 16, 32 or 64) over M.  The (n-tile, k-block) units are split
 // into G contiguous ranges, one per CTA; tiles cut across ranges are summed
 // in a fixed order by the last CTA to finish one of their pieces.
-template <int MN_, int STAGES_>
+template <int MN_>
 struct SkinnyConfig {
     static constexpr int MN = MN_;
-    static constexpr int STAGES = STAGES_;
     static constexpr int W_BYTES = 128 * kBK * 2;   // weight (B) tile: 128 rows
     static constexpr int X_BYTES = MN * kBK * 2;    // activation (A) tile: MN rows
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    // This kernel streams B once and is bound by how many bytes are in flight,
+    // so the ring takes every stage that fits beside the barriers (12 / 11 / 9).
+    static constexpr int STAGES = (kMaxDynSmem - 2048) / STAGE_BYTES;
     static constexpr int TMEM_COLS = (2 * MN < 32) ? 32 : 2 * MN;
     static constexpr int OFF_W = 0;
     static constexpr int OFF_X = OFF_W + STAGES * W_BYTES;
@@ -113,13 +162,14 @@ struct SkinnyConfig {
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
     static constexpr uint32_t IDESC = ptx::idesc_f16_f32(128, MN);
     static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
+    static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
 };
 
-using CfgSkinny16 = SkinnyConfig<16, 8>;
-using CfgSkinny32 = SkinnyConfig<32, 8>;
-using CfgSkinny64 = SkinnyConfig<64, 8>;
+using CfgSkinny16 = SkinnyConfig<16>;
+using CfgSkinny32 = SkinnyConfig<32>;
+using CfgSkinny64 = SkinnyConfig<64>;
 
 struct SkinnyParams {
     int32_t M, N, K;

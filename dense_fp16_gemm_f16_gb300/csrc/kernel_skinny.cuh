@@ -192,7 +192,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 float* mine = p.partials +
                               ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
 #pragma unroll
-                for (int m = 0; m < MN; ++m) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
+                for (int m = 0; m < MN; ++m)
+                    if (m < p.M) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
                 __threadfence();
                 ptx::named_bar_sync(1, 32 * kEpiWarps);
                 if (etid == 0) {
@@ -203,14 +204,36 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 if (*last_flag) {
                     __threadfence();
                     if (n < p.N) {
-                        for (int m = 0; m < MN && m < p.M; ++m) {
-                            float acc = 0.0f;
-                            for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                                const int64_t j = t - unit_begin(cc, W, G) / KB;
-                                acc += __ldcg(p.partials + ((cc * p.max_tiles_per_cta + j) * MN + m) * 128 + r);
+                        // Sum the pieces in ascending CTA order.  Pieces are fetched
+                        // CH at a time with independent loads so their latencies
+                        // overlap; the additions keep the fixed order.
+                        constexpr int CH = 64 / MN;
+                        float acc[MN];
+#pragma unroll
+                        for (int m = 0; m < MN; ++m) acc[m] = 0.0f;
+                        for (int64_t c0 = c_first; c0 <= c_last; c0 += CH) {
+                            float pv[CH][MN];
+#pragma unroll
+                            for (int i = 0; i < CH; ++i) {
+                                const int64_t cc = c0 + i;
+                                const bool have = cc <= c_last;
+                                const int64_t j = have ? t - unit_begin(cc, W, G) / KB : 0;
+                                const float* src =
+                                    p.partials + ((cc * p.max_tiles_per_cta + j) * MN) * 128 + r;
+#pragma unroll
+                                for (int m = 0; m < MN; ++m)
+                                    pv[i][m] = (have && m < p.M) ? __ldcg(src + m * 128) : 0.0f;
                             }
-                            D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(acc);
+#pragma unroll
+                            for (int i = 0; i < CH; ++i)
+                                if (c0 + i <= c_last) {
+#pragma unroll
+                                    for (int m = 0; m < MN; ++m) acc[m] += pv[i][m];
+                                }
                         }
+#pragma unroll
+                        for (int m = 0; m < MN; ++m)
+                            if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(acc[m]);
                     }
                     if (etid == 0) p.counters[t] = 0u;  // re-armed for the next call on this stream
                 }

@@ -90,11 +90,13 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
-            for (int64_t t = cluster_idx; ok && t < p.num_tiles; t += num_clusters) {
-                int64_t tm, tn;
-                tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+            for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters) {
+                int64_t tm, n0;
+                int nw;
+                work_unit(u, p, Cfg::BN, tm, n0, nw);
+                // each CTA of a pair supplies nw / CG rows of B to the MMA
                 const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * Cfg::A_ROWS);
-                const int32_t b_row = static_cast<int32_t>(tn * Cfg::BN + rank * Cfg::B_ROWS);
+                const int32_t b_row = static_cast<int32_t>(n0 + rank * (nw / CG));
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
                                     p.timeout_ns)) {
@@ -132,7 +134,11 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0;
             uint32_t phase = 0;
             uint32_t it = 0;
-            for (int64_t t = cluster_idx; ok && t < p.num_tiles; t += num_clusters, ++it) {
+            for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters, ++it) {
+                int64_t tm, n0;
+                int nw;
+                work_unit(u, p, Cfg::BN, tm, n0, nw);
+                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::BM, nw);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
                 // the epilogue must have drained this accumulator buffer
@@ -154,7 +160,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int k = 0; k < kBK / 16; ++k) {
                         // +32 bytes (2 in the >>4 address field) per 16-wide K step;
                         // the first product of a tile overwrites the accumulator.
-                        ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                        ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                          (kb | k) != 0 ? 1u : 0u);
                     }
                     // release the stage to the producers once these MMAs have read it
@@ -179,9 +185,11 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(tempty_bar(0), 0) : tempty_bar(0);
         uint32_t it = 0;
         int ebuf = 0;
-        for (int64_t t = cluster_idx; t < p.num_tiles; t += num_clusters, ++it) {
-            int64_t tm, tn;
-            tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+        for (int64_t u = cluster_idx; u < p.num_units; u += num_clusters, ++it) {
+            int64_t tm, n0;
+            int nw;
+            work_unit(u, p, Cfg::BN, tm, n0, nw);
+            const int chunks = nw / Cfg::EPI_COLS;
             const uint32_t buf = it & 1u;
             const uint32_t use = (it >> 1) & 1u;
             if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns))
@@ -191,12 +199,12 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool rows_in = row0 < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
 #pragma unroll 1
-            for (int c = 0; c < Cfg::BN / Cfg::EPI_COLS; ++c) {
+            for (int c = 0; c < chunks; ++c) {
                 uint32_t v[64];
                 ptx::tmem_ld_x32(t_row + c * 64, v);
                 ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
                 ptx::tmem_wait_ld();
-                if (c == Cfg::BN / Cfg::EPI_COLS - 1) {
+                if (c == chunks - 1) {
                     // this warp has read its part of the buffer: return it to the MMA
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -205,7 +213,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         else ptx::mbar_arrive(tempty_bar(buf));
                     }
                 }
-                const int64_t col0 = tn * Cfg::BN + c * Cfg::EPI_COLS;
+                const int64_t col0 = n0 + c * Cfg::EPI_COLS;
                 const bool store = rows_in && col0 < p.N;  // warp-uniform
                 // the TMA store issued two chunks ago from this buffer has read it
                 if (lane == 0) ptx::bulk_wait_group_read<1>();

@@ -131,6 +131,9 @@ typedef struct {
     int32_t tmem_cols;       /* TMEM columns allocated per CTA */
     int32_t max_tiles_per_cta; /* skinny: partial-sum slots per CTA, else 0 */
     int64_t workspace_bytes; /* skinny: fp32 partials + counters, else 0 */
+    int64_t num_full_tiles;  /* tiled: tiles run whole (the persistent grid's full rounds) */
+    int32_t tail_split;      /* tiled: the other tiles are cut into this many column pieces */
+    int32_t group_m;         /* tiled: tile rows per raster group (L2 reuse of A) */
 } gemm_plan_t;
 
 /*

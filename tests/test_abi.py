@@ -113,13 +113,21 @@ def test_plans_for_the_named_workloads(lib):
     assert p["variant"] == "TILE_2CTA_256x256" and p["cta_group"] == 2
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 32, 128)
     assert p["grid_ctas"] == 152 and p["tmem_cols"] == 512
+    # 1024 tiles on 76 pairs: 13 whole rounds (988 tiles), the last 36 tiles cut
+    # in halves (72 pieces on 76 pairs) instead of a 14th round of 36 tiles
+    assert (p["num_full_tiles"], p["tail_split"]) == (988, 2)
+    assert p["group_m"] == 8                 # 8 x 256 rows x 16 KB = 32 MiB of A per group (34 MiB budget)
     p = P(4000, 11000, 4104)
     assert p["variant"] == "TILE_2CTA_256x256"
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)   # ragged in M, N and K
+    assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds + 4 tiles in quarters
+    assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
     p = P(1024, 1024, 2048)
-    assert p["variant"] == "TILE_1CTA_128x128" and p["grid_ctas"] == 64
+    assert p["variant"] == "TILE_1CTA_128x128"
+    assert (p["num_full_tiles"], p["tail_split"], p["grid_ctas"]) == (0, 2, 128)
     p = P(128, 128, 64)
-    assert p["variant"] == "TILE_1CTA_128x128" and p["grid_ctas"] == 1 and p["k_blocks"] == 1
+    assert p["variant"] == "TILE_1CTA_128x128" and p["k_blocks"] == 1
+    assert (p["tail_split"], p["grid_ctas"]) == (2, 2)
     p = P(16, 8192, 8192)
     assert p["variant"] == "SKINNY_SPLITK" and p["tile_m"] == 16 and p["n_tiles"] == 64
     assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 2
@@ -141,6 +149,26 @@ def test_skinny_split_covers_every_unit_once(lib):
     # many tiles with short K: each CTA owns several whole tiles
     p = g.gemm_f16_nt_plan(16, 65536, 64, num_sms=152)
     assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 4   # 512 whole tiles over 152 CTAs
+
+
+def test_tail_split_minimises_the_last_round(lib):
+    # whole rounds first; the remainder is cut into 1, 2 or 4 column pieces,
+    # whichever gives the shortest tail (ties keep fewer pieces)
+    cases = {  # (M, N) on 76 pairs of 256x256 tiles -> (num_full, split)
+        (256 * 76, 256): (76, 1),          # exactly one round
+        (256 * 77, 256): (76, 4),          # one tile left: quarters
+        (256 * 38, 512): (76, 1),          # 76 tiles
+        (256 * 50, 256): (0, 1),           # 50 tiles: halves would still take one round
+        (256 * 100, 256): (76, 2),         # 24 left: halves fit in one round (48 <= 76)
+    }
+    for (M, N), want in cases.items():
+        p = g.gemm_f16_nt_plan(M, N, 64, g.Variant.TILE_2CTA_256x256, num_sms=152)
+        assert (p["num_full_tiles"], p["tail_split"]) == want, (M, N, p)
+        units = p["num_full_tiles"] + (p["m_tiles"] * p["n_tiles"] - p["num_full_tiles"]) * p["tail_split"]
+        assert p["grid_ctas"] == 2 * min(units, 76)
+    # 128-wide tiles are cut at most in halves (pieces stay >= 64 columns)
+    p = g.gemm_f16_nt_plan(128 * 153, 128, 64, g.Variant.TILE_1CTA_128x128, num_sms=152)
+    assert (p["num_full_tiles"], p["tail_split"]) == (152, 2)
 
 
 def test_plan_errors(lib):
