@@ -82,6 +82,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT);
+    // Everything above touched only this CTA's shared memory and TMEM, so it
+    // overlaps the previous kernel's tail; global memory is used only below.
+    // (Every kernel here takes more than half of an SM's shared memory, so a
+    // CTA of this grid never shares an SM, or its TMEM, with one of the last.)
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
 
     const int64_t G = p.num_ctas;
     const int64_t W = p.units;
@@ -189,19 +195,34 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(__uint_as_float(v[m]));
                 }
             } else {
-                float* mine = p.partials +
-                              ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
-#pragma unroll
-                for (int m = 0; m < MN; ++m)
-                    if (m < p.M) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
-                __threadfence();
-                ptx::named_bar_sync(1, 32 * kEpiWarps);
-                if (etid == 0) {
-                    const uint32_t prev = atomicAdd(p.counters + t, 1u);
-                    *last_flag = (prev == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+                // The piece holding k = 0 ends the range of the CTA before the
+                // tile's other pieces, so it usually finishes last.  Its owner
+                // checks first: if every other piece is already in, it adds them
+                // to its own values directly (no write and re-read of its own
+                // partial).  Otherwise -- and always for the other pieces -- the
+                // piece is published and the last to arrive sums the tile.
+                const bool owner = (c == c_first);
+                if (owner && etid == 0) {
+                    const uint32_t done = atomicAdd(p.counters + t, 0u);
+                    *last_flag = (done == static_cast<uint32_t>(c_last - c_first)) ? 2u : 0u;
                 }
-                ptx::named_bar_sync(1, 32 * kEpiWarps);
+                if (owner) ptx::named_bar_sync(1, 32 * kEpiWarps);
+                if (!(owner && *last_flag == 2u)) {
+                    float* mine = p.partials +
+                                  ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
+#pragma unroll
+                    for (int m = 0; m < MN; ++m)
+                        if (m < p.M) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
+                    __threadfence();
+                    ptx::named_bar_sync(1, 32 * kEpiWarps);
+                    if (etid == 0) {
+                        const uint32_t prev = atomicAdd(p.counters + t, 1u);
+                        *last_flag = (prev == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+                    }
+                    ptx::named_bar_sync(1, 32 * kEpiWarps);
+                }
                 if (*last_flag) {
+                    const bool self_in_regs = (*last_flag == 2u);
                     __threadfence();
                     if (n < p.N) {
                         // Sum the pieces in ascending CTA order.  Pieces are fetched
@@ -217,12 +238,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                             for (int i = 0; i < CH; ++i) {
                                 const int64_t cc = c0 + i;
                                 const bool have = cc <= c_last;
+                                const bool in_regs = self_in_regs && cc == c;   // own piece, not published
                                 const int64_t j = have ? t - unit_begin(cc, W, G) / KB : 0;
                                 const float* src =
                                     p.partials + ((cc * p.max_tiles_per_cta + j) * MN) * 128 + r;
 #pragma unroll
                                 for (int m = 0; m < MN; ++m)
-                                    pv[i][m] = (have && m < p.M) ? __ldcg(src + m * 128) : 0.0f;
+                                    pv[i][m] = in_regs ? __uint_as_float(v[m])
+                                               : (have && m < p.M) ? __ldcg(src + m * 128) : 0.0f;
                             }
 #pragma unroll
                             for (int i = 0; i < CH; ++i)

@@ -80,6 +80,12 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT);
+    // Everything above touched only this CTA's shared memory and TMEM, so it
+    // overlaps the previous kernel's tail; global memory is used only below.
+    // (Every kernel here takes more than half of an SM's shared memory, so a
+    // CTA of this grid never shares an SM, or its TMEM, with one of the last.)
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
 
     const int64_t cluster_idx = blockIdx.x / CG;
     const int64_t num_clusters = gridDim.x / CG;

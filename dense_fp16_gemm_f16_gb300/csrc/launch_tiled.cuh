@@ -40,14 +40,19 @@ struct TiledLauncher {
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        cfg.numAttrs = 0;
+        // programmatic stream serialisation: this grid may be scheduled while the
+        // previous kernel in the stream finishes; it waits (griddepcontrol.wait)
+        // before its first global access
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
         if constexpr (Cfg::CG == 2) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.numAttrs = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = 2;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
         }
         cfg.attrs = attr;
         return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg>, a, b, d, p);

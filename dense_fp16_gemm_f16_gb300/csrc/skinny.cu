@@ -18,8 +18,11 @@ struct SkinnyLauncher {
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
-        cfg.numAttrs = 0;
-        cfg.attrs = nullptr;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+        cfg.attrs = attr;
         return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<Cfg>, w, x, p);
     }
     static const SkinnyOps& ops() {
