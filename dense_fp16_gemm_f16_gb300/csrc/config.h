@@ -47,16 +47,21 @@ struct TiledConfig {
     static constexpr int TMEM_COLS = 2 * BN;                 // two accumulator buffers
     static constexpr int EPI_COLS = 64;                      // columns per TMA store box
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // one warp's 32 rows
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    // The operand ring holds STAGES whole stages of [A tile | B tile].  A launch
+    // made only of column pieces (see tail_split) needs only B_BYTES / split of
+    // B per stage, so it packs more, smaller stages into the same ring: more
+    // bytes in flight for the latency-bound small problems.
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int MAX_SPLIT = (BN / 64 < 4) ? BN / 64 : 4;
+    static constexpr int MAX_STAGES = RING_BYTES / (A_BYTES + B_BYTES / MAX_SPLIT);
+    static constexpr int OFF_EPI = RING_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 2 * EPI_BUF_BYTES;
-    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    // full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2], drain
+    static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;  // + slack to align the base
     static constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
-    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
+    static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT) % 1024 == 0, "stage tiles must stay 1024-aligned");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 up to 256");
     static_assert(B_ROWS <= 256, "TMA box rows are limited to 256");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
@@ -93,6 +98,12 @@ GEMM_HD void tile_coords(int64_t t, int64_t m_tiles, int64_t n_tiles, int64_t gr
     const int64_t r = t - g * per_group;
     tm = first_m + r % rows;
     tn = r / rows;
+}
+
+// Bytes per ring stage of a launch: a whole [A | B] stage, or, when every
+// unit is a column piece (no whole tiles), [A | B / split].
+GEMM_HD int ring_stride(const TiledParams& p, int a_bytes, int b_bytes) {
+    return (p.num_full == 0 && p.split > 1) ? a_bytes + b_bytes / p.split : a_bytes + b_bytes;
 }
 
 // Work unit u of the persistent loop -> (tile row tm, first column n0,

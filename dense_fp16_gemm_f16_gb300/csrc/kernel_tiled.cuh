@@ -35,9 +35,10 @@ namespace gemm_gb300 {
 template <class Cfg>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmD, const TiledParams p) {
+                  const __grid_constant__ CUtensorMap tmBpiece, const __grid_constant__ CUtensorMap tmD,
+                  const TiledParams p) {
     constexpr int CG = Cfg::CG;
-    constexpr int STAGES = Cfg::STAGES;
+    constexpr int MAXS = Cfg::MAX_STAGES;
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1024 bytes (the 128-byte swizzle atom); every
     // CTA of a pair gets the same offsets, which the pair MMA relies on.
@@ -51,17 +52,21 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const uint32_t bar0 = sbase + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (MAXS + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * MAXS + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * MAXS + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * MAXS + 4);
+    // ring geometry of this launch (the same in every role and both CTAs of a pair)
+    const uint32_t stride = static_cast<uint32_t>(ring_stride(p, Cfg::A_BYTES, Cfg::B_BYTES));
+    const int STAGES = static_cast<int>(Cfg::RING_BYTES / stride);
     const uint32_t slot = sbase + Cfg::OFF_SLOT;
 
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmBpiece);
         ptx::prefetch_tensormap(&tmD);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < MAXS; ++s) {
             ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival + TMA bytes
             ptx::mbar_init(empty_bar(s), 1);  // one MMA commit
         }
@@ -100,28 +105,33 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 int64_t tm, n0;
                 int nw;
                 work_unit(u, p, Cfg::BN, tm, n0, nw);
-                // each CTA of a pair supplies nw / CG rows of B to the MMA
+                // each CTA of a pair supplies nw / CG rows of B to the MMA; a
+                // column piece of a tail tile loads only those rows (box of the
+                // second B map) instead of the whole tile's
                 const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * Cfg::A_ROWS);
                 const int32_t b_row = static_cast<int32_t>(n0 + rank * (nw / CG));
+                const bool piece = nw < Cfg::BN;
+                const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
+                const uint32_t stage_bytes = Cfg::A_BYTES + (piece ? Cfg::B_BYTES / p.split : Cfg::B_BYTES);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
                                     p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a_dst = sbase + Cfg::OFF_A + stage * Cfg::A_BYTES;
-                    const uint32_t b_dst = sbase + Cfg::OFF_B + stage * Cfg::B_BYTES;
+                    const uint32_t a_dst = sbase + stage * stride;
+                    const uint32_t b_dst = a_dst + Cfg::A_BYTES;
                     if constexpr (CG == 1) {
-                        ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
                         ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, a_row);
-                        ptx::tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, b_row);
+                        ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kb * kBK, b_row);
                     } else {
                         // Both CTAs' bytes complete on the leader's full barrier; the
                         // leader announces the pair's total.
                         const uint32_t leader_full = ptx::mapa(full_bar(stage), 0);
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
                         ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
-                        ptx::tma_load_2d_pair(b_dst, &tmB, leader_full, kb * kBK, b_row);
+                        ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kb * kBK, b_row);
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -160,8 +170,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_A + stage * Cfg::A_BYTES);
-                    const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_B + stage * Cfg::B_BYTES);
+                    const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + stage * stride);
+                    const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + stage * stride + Cfg::A_BYTES);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         // +32 bytes (2 in the >>4 address field) per 16-wide K step;

@@ -16,8 +16,10 @@ struct TiledOps {
     cudaError_t (*prepare)();
     // co-resident clusters (cta_group 2) or CTAs per SM (cta_group 1) on the current device
     cudaError_t (*max_active)(int* out);
-    cudaError_t (*launch)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                          const TiledParams& p, int grid_ctas, cudaStream_t stream);
+    // b_piece: B with a box of (B rows per CTA) / split rows, for the column
+    // pieces of the last round's tiles
+    cudaError_t (*launch)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_piece,
+                          const CUtensorMap& d, const TiledParams& p, int grid_ctas, cudaStream_t stream);
 };
 
 struct SkinnyOps {

@@ -33,8 +33,8 @@ struct TiledLauncher {
         }
     }
 
-    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                              const TiledParams& p, int grid_ctas, cudaStream_t stream) {
+    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_piece,
+                              const CUtensorMap& d, const TiledParams& p, int grid_ctas, cudaStream_t stream) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
@@ -55,7 +55,7 @@ struct TiledLauncher {
             cfg.numAttrs = 2;
         }
         cfg.attrs = attr;
-        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg>, a, b, d, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg>, a, b, b_piece, d, p);
     }
 
     static const TiledOps& ops() {

@@ -123,8 +123,8 @@ def test_plans_for_the_named_workloads(lib):
     assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds + 4 tiles in quarters
     assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
     p = P(1024, 1024, 2048)
-    assert p["variant"] == "TILE_1CTA_128x128"
-    assert (p["num_full_tiles"], p["tail_split"], p["grid_ctas"]) == (0, 2, 128)
+    assert p["variant"] == "TILE_1CTA_128x256"                          # 32 tiles, cut in quarters
+    assert (p["num_full_tiles"], p["tail_split"], p["grid_ctas"]) == (0, 4, 128)
     p = P(128, 128, 64)
     assert p["variant"] == "TILE_1CTA_128x128" and p["k_blocks"] == 1
     assert (p["tail_split"], p["grid_ctas"]) == (2, 2)
