@@ -40,6 +40,7 @@ class Variant(enum.IntEnum):
     TILE_1CTA_128x128 = 2
     TILE_1CTA_128x256 = 3
     SKINNY_SPLITK = 4
+    TILE_2CTA_SPLITK = 5
 
 
 class LibraryMissing(RuntimeError):
@@ -61,6 +62,7 @@ class Plan(ctypes.Structure):
         ("grid_ctas", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
         ("max_tiles_per_cta", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
         ("num_full_tiles", ctypes.c_int64), ("tail_split", ctypes.c_int32), ("group_m", ctypes.c_int32),
+        ("k_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -56,6 +56,8 @@ constexpr int64_t kMaxDim = INT32_MAX;
 // B blocks stream past (measured best: 8 tile rows at K = 8192, all 16 at
 // 4000 x 11000 x 4104).  GEMM_GROUP_M fixes the group size instead.
 constexpr int64_t kL2GroupBytes = 34ll << 20;
+// AUTO uses split-K for the pair kernel only from this many K blocks up.
+constexpr int64_t kSplitKMinBlocks = 40;
 
 int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K) {
 #ifdef GEMM_GROUP_M
@@ -91,9 +93,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     std::memset(pl, 0, sizeof(*pl));
     const gemm_status_t st = check_sizes(M, N, K);
     if (st != GEMM_OK) return st;
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
+    const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
 
     if (variant == GEMM_VARIANT_AUTO) {
         if (M <= 64) {
@@ -105,9 +108,16 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // (Measured on GB300: e.g. 2048^3 14.1 us on 128x256 vs 15.7 us on
             // pairs and 20.3 us on 128x128; 4000x11000x4104 253 us on pairs vs
             // 350 us on 128x256.)
+            // With at most half a round of pair tiles and a long K loop, split
+            // each tile's K loop over several pairs instead (fewer, larger
+            // tiles: less L2 traffic).  Publishing and re-reading the fp32
+            // partials costs a fixed ~8 us, so short K loops stay unsplit
+            // (measured on GB300: 512x2048x8192 22.9 us split vs 39.1 us on
+            // 128x256 tiles; 1024x1024x2048 15.8 us split vs 12.7 us).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
-            const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
             if (t2 >= pairs) variant = GEMM_VARIANT_TILE_2CTA_256x256;
+            else if (cdiv(K, kBK) >= kSplitKMinBlocks && choose_ksplit(t2, pairs, cdiv(K, kBK)) > 1)
+                variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
             else if (cdiv(M, 128) * cdiv(N, 256) >= 2) variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else variant = GEMM_VARIANT_TILE_1CTA_128x128;
         }
@@ -142,7 +152,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
         return GEMM_OK;
     }
 
-    const TiledOps& ops = variant == GEMM_VARIANT_TILE_2CTA_256x256 ? tiled_ops_2cta256()
+    if (variant == GEMM_VARIANT_TILE_2CTA_SPLITK &&
+        choose_ksplit(cdiv(M, 256) * cdiv(N, 256), pairs, pl->k_blocks) < 2)
+        variant = GEMM_VARIANT_TILE_2CTA_256x256;   // enough tiles already: no split
+    pl->variant = variant;
+    const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK;
+    const TiledOps& ops = (variant == GEMM_VARIANT_TILE_2CTA_256x256 || ksplit_variant) ? tiled_ops_2cta256()
                           : variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
                                                                       : tiled_ops_1cta256();
     pl->cta_group = ops.cta_group;
@@ -166,8 +181,17 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     if (slots <= 0) return GEMM_ERR_INVALID_VALUE;
     int64_t num_full;
     int split;
-    tail_split(tiles, slots, ops.tile_n, ops.cta_group, num_full, split);
-    const int64_t units = num_full + (tiles - num_full) * split;
+    int ksplit = 1;
+    if (ksplit_variant) {
+        ksplit = choose_ksplit(tiles, slots, pl->k_blocks);
+        num_full = tiles;
+        split = 1;
+        pl->workspace_bytes = round_up(tiles * ksplit * ops.tile_m * ops.tile_n * 4, 256) + round_up(tiles * 4, 256);
+    } else {
+        tail_split(tiles, slots, ops.tile_n, ops.cta_group, num_full, split);
+    }
+    pl->k_split = ksplit;
+    const int64_t units = ksplit > 1 ? tiles * ksplit : num_full + (tiles - num_full) * split;
     const int64_t clusters = units < slots ? units : slots;
     pl->grid_ctas = static_cast<int32_t>(clusters * ops.cta_group);
     pl->num_full_tiles = num_full;
@@ -316,7 +340,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     // ---- host-only argument checks (nothing touches a device before these pass)
     gemm_status_t st = check_sizes(M, N, K);
     if (st != GEMM_OK) return st;
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
@@ -374,9 +398,17 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         return GEMM_OK;
     }
 
-    const TiledOps& ops = pl.variant == GEMM_VARIANT_TILE_2CTA_256x256 ? tiled_ops_2cta256()
+    const TiledOps& ops = (pl.variant == GEMM_VARIANT_TILE_2CTA_256x256 || pl.variant == GEMM_VARIANT_TILE_2CTA_SPLITK)
+                              ? tiled_ops_2cta256()
                           : pl.variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
                                                                          : tiled_ops_1cta256();
+    Workspace* ws = nullptr;
+    if (pl.k_split > 1) {
+        const size_t partial_bytes = static_cast<size_t>(pl.m_tiles * pl.n_tiles) * pl.k_split * ops.tile_m *
+                                     ops.tile_n * sizeof(float);
+        st = get_workspace(dev_id, stream, partial_bytes, static_cast<size_t>(pl.m_tiles * pl.n_tiles), &ws);
+        if (st != GEMM_OK) return st;
+    }
     CUtensorMap ta, tb, tbp, td;
     const uint32_t b_rows = static_cast<uint32_t>(ops.tile_n / ops.cta_group);
     if (!encode_2d(&ta, A, K, M, kBK, 128) || !encode_2d(&tb, B, K, N, kBK, b_rows) ||
@@ -394,8 +426,12 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.group_m = pl.group_m;
     p.num_full = pl.num_full_tiles;
     p.split = pl.tail_split;
-    p.reserved = 0;
-    p.num_units = pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
+    p.ksplit = pl.k_split;
+    p.num_units = pl.k_split > 1 ? p.num_tiles * pl.k_split
+                                 : pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
+    p.partials = ws ? ws->partials : nullptr;
+    p.counters = ws ? ws->counters : nullptr;
+    p.D = D;
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
     if (ops.launch(ta, tb, tbp, td, p, pl.grid_ctas, s) != cudaSuccess) {

@@ -81,7 +81,10 @@ struct TiledParams {
     int64_t num_full;         // tiles run whole: the persistent grid's full rounds
     int64_t num_units;        // num_full + (num_tiles - num_full) * split
     int32_t split;            // the remaining tiles are cut into `split` column pieces
-    int32_t reserved;
+    int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces (split-K)
+    float* partials;          // split-K: [num_tiles][ksplit][BM][BN] fp32
+    uint32_t* counters;       // split-K: [num_tiles], zero between calls
+    void* D;                  // split-K: the output, written by the slice reductions
     uint32_t* status;         // device status word (0 = ok)
     uint64_t timeout_ns;      // per-wait budget
 };
@@ -110,7 +113,22 @@ GEMM_HD int ring_stride(const TiledParams& p, int a_bytes, int b_bytes) {
 // column count nw).  The first num_full units are whole tiles in raster
 // order; the tiles of the last, partly filled round are cut into `split`
 // column pieces so that more CTA pairs share that round.
-GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int64_t& n0, int& nw) {
+GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int64_t& n0, int& nw,
+                       int& kb0, int& kb1) {
+    kb0 = 0;
+    kb1 = p.k_blocks;
+    if (p.ksplit > 1) {
+        // split-K: unit u is piece j of tile t; the pieces split the K blocks evenly
+        const int64_t t = u / p.ksplit;
+        const int j = static_cast<int>(u - t * p.ksplit);
+        int64_t tn;
+        tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
+        nw = BN;
+        n0 = tn * BN;
+        kb0 = static_cast<int>(static_cast<int64_t>(j) * p.k_blocks / p.ksplit);
+        kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.k_blocks / p.ksplit);
+        return;
+    }
     int64_t t = u, piece = 0;
     int s = 1;
     if (u >= p.num_full) {
@@ -147,6 +165,17 @@ inline void tail_split(int64_t num_tiles, int64_t slots, int BN, int CG, int64_t
             split = s;
         }
     }
+}
+
+// Split-K factor for the pair kernel when its tiles do not fill a round of
+// CTA pairs: as many pieces per tile as keep every unit resident at once
+// (tiles * S <= slots), at most 8, and at least 4 K blocks per piece.
+inline int choose_ksplit(int64_t tiles, int64_t slots, int64_t k_blocks) {
+    if (tiles <= 0 || tiles * 2 > slots) return 1;
+    int64_t s = slots / tiles;
+    if (s > 8) s = 8;
+    if (s > k_blocks / 4) s = k_blocks / 4;
+    return s < 2 ? 1 : static_cast<int>(s);
 }
 
 // ------------------------------------------------------------------ skinny

@@ -32,6 +32,157 @@
 
 namespace gemm_gb300 {
 
+// Split-K partials of one piece are stored in a blocked column-major layout,
+// [BN/4 column quads][BM rows][4 columns] fp32: a thread (one row) moves four
+// consecutive columns with one 16-byte access, and the 32 lanes of a warp
+// (32 consecutive rows) cover one contiguous 512-byte run.
+template <int BM>
+__device__ __forceinline__ int64_t split_quad_offset(int col, int row) {
+    return (static_cast<int64_t>(col >> 2) * BM + row) * 4;
+}
+
+// Sum of the S pieces of this thread's row over columns [c_begin, c_end) (a
+// multiple of 8 wide), pieces in ascending order, written to D as fp16.
+// Loads go out in batches of up to 8 float4 (two 8-column groups when S = 2,
+// else one group with up to 4 pieces) before the additions that use them.
+template <class Cfg, int S>
+__device__ __forceinline__ void split_k_reduce_row(const float* base, int r_local, int c_begin, int c_end,
+                                                   int64_t n0, int64_t grow, const TiledParams& p) {
+    constexpr int GB = (S <= 2) ? 2 : 1;            // 8-column groups per batch
+    constexpr int JC = (S < 4) ? S : 4;             // pieces per batch
+    const int64_t piece_stride = static_cast<int64_t>(Cfg::BM) * Cfg::BN;
+    __half* D = static_cast<__half*>(p.D);
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 8 * GB) {
+        float acc[GB][8];
+#pragma unroll
+        for (int g = 0; g < GB; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] = 0.0f;
+#pragma unroll
+        for (int j0 = 0; j0 < S; j0 += JC) {
+            float4 pv[GB][JC][2];
+#pragma unroll
+            for (int g = 0; g < GB; ++g) {
+                const int cg = c + 8 * g;
+#pragma unroll
+                for (int jj = 0; jj < JC; ++jj) {
+                    if (j0 + jj < S && cg < c_end) {
+                        const float* src = base + (j0 + jj) * piece_stride;
+                        pv[g][jj][0] = __ldcg(reinterpret_cast<const float4*>(src + split_quad_offset<Cfg::BM>(cg, r_local)));
+                        pv[g][jj][1] = __ldcg(reinterpret_cast<const float4*>(src + split_quad_offset<Cfg::BM>(cg + 4, r_local)));
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < GB; ++g) {
+#pragma unroll
+                for (int jj = 0; jj < JC; ++jj) {
+                    if (j0 + jj < S && c + 8 * g < c_end) {
+                        acc[g][0] += pv[g][jj][0].x; acc[g][1] += pv[g][jj][0].y;
+                        acc[g][2] += pv[g][jj][0].z; acc[g][3] += pv[g][jj][0].w;
+                        acc[g][4] += pv[g][jj][1].x; acc[g][5] += pv[g][jj][1].y;
+                        acc[g][6] += pv[g][jj][1].z; acc[g][7] += pv[g][jj][1].w;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+            const int cg = c + 8 * g;
+            const int64_t gcol = n0 + cg;
+            if (cg < c_end && gcol < p.N) {         // N % 8 == 0: groups are all in or all out
+                uint32_t h[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __half2 x = __floats2half2_rn(acc[g][2 * e], acc[g][2 * e + 1]);
+                    h[e] = *reinterpret_cast<const uint32_t*>(&x);
+                }
+                *reinterpret_cast<uint4*>(D + grow * static_cast<int64_t>(p.N) + gcol) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+            }
+        }
+    }
+}
+
+// Split-K epilogue of one unit (piece j of tile t), run by the four epilogue
+// warps of each CTA of the pair: publish this piece's fp32 partial (this CTA's
+// 128 rows), wait until every piece of the tile is in, then sum all pieces of
+// this CTA's rows over the unit's 1/ksplit slice of columns -- pieces in
+// ascending order, so the result does not depend on timing -- and store that
+// slice of D.  The last CTA through re-arms the tile's counter.
+template <class Cfg>
+__device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u, int64_t tm, int64_t n0,
+                                                 uint32_t t_row, uint32_t tempty_leader0, uint32_t tempty_local,
+                                                 uint32_t buf, int q, int lane, int etid, uint32_t rank) {
+    constexpr int CG = Cfg::CG;
+    constexpr int BN = Cfg::BN;
+    const int S = p.ksplit;
+    const int64_t t = u / S;
+    const int j = static_cast<int>(u - t * S);
+    const int r_local = static_cast<int>(rank) * 128 + q * 32 + lane;     // row within the pair's tile
+    // 1. partial of this piece: TMEM -> registers -> workspace
+    float* piece = p.partials + (t * S + j) * static_cast<int64_t>(BN) * Cfg::BM;
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+        uint32_t v[64];
+        ptx::tmem_ld_x32(t_row + c * 64, v);
+        ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
+        ptx::tmem_wait_ld();
+        if (c == BN / 64 - 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2) ptx::mbar_arrive_cluster(tempty_leader0 + 8u * buf);
+                else ptx::mbar_arrive(tempty_local);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            __stcg(reinterpret_cast<float4*>(piece + split_quad_offset<Cfg::BM>(c * 64 + 4 * i, r_local)),
+                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+    }
+    __threadfence();
+    ptx::named_bar_sync(1, 32 * kEpiWarps);
+    // 2. every piece of the tile (S pieces x CG CTAs) is in
+    const uint32_t pieces = static_cast<uint32_t>(S * CG);
+    bool ready = true;
+    if (etid == 0) {
+        atomicAdd(p.counters + t, 1u);
+        ready = wait_count(p.counters + t, pieces, p.status, kSiteSplitPieces, p.timeout_ns);
+    }
+    if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) return false;
+    __threadfence();
+    // 3. this unit's slice of columns, summed over the pieces in ascending order.
+    // The tile's BN / 8 groups of 8 columns are dealt out to the S units, so
+    // every slice starts on a multiple of 8 (16-byte fp16 stores, 32-byte fp32
+    // loads) and the slices cover all BN columns for any S <= 8.
+    constexpr int kGroups = BN / 8;
+    const int c_begin = 8 * (j * kGroups / S);
+    const int c_end = 8 * ((j + 1) * kGroups / S);
+    const int64_t grow = tm * Cfg::BM + r_local;    // D row
+    if (grow < p.M) {
+        const float* base = p.partials + t * S * static_cast<int64_t>(BN) * Cfg::BM;
+        switch (S) {
+            case 2: split_k_reduce_row<Cfg, 2>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 3: split_k_reduce_row<Cfg, 3>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 4: split_k_reduce_row<Cfg, 4>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 5: split_k_reduce_row<Cfg, 5>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 6: split_k_reduce_row<Cfg, 6>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 7: split_k_reduce_row<Cfg, 7>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            default: split_k_reduce_row<Cfg, 8>(base, r_local, c_begin, c_end, n0, grow, p); break;
+        }
+    }
+    // 4. the last of the 2 * S * CG arrivals re-arms the counter for the next call
+    ptx::named_bar_sync(1, 32 * kEpiWarps);
+    if (etid == 0) {
+        const uint32_t prev = atomicAdd(p.counters + t, 1u);
+        if (prev == 2u * pieces - 1u) p.counters[t] = 0u;
+    }
+    return true;
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -103,8 +254,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters) {
                 int64_t tm, n0;
-                int nw;
-                work_unit(u, p, Cfg::BN, tm, n0, nw);
+                int nw, kb0, kb1;
+                work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
                 // each CTA of a pair supplies nw / CG rows of B to the MMA; a
                 // column piece of a tail tile loads only those rows (box of the
                 // second B map) instead of the whole tile's
@@ -113,7 +264,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const bool piece = nw < Cfg::BN;
                 const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
                 const uint32_t stage_bytes = Cfg::A_BYTES + (piece ? Cfg::B_BYTES / p.split : Cfg::B_BYTES);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
                                     p.timeout_ns)) {
                         ok = false;
@@ -152,8 +303,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t it = 0;
             for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters, ++it) {
                 int64_t tm, n0;
-                int nw;
-                work_unit(u, p, Cfg::BN, tm, n0, nw);
+                int nw, kb0, kb1;
+                work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
                 const uint32_t idesc = ptx::idesc_f16_f32(Cfg::BM, nw);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
@@ -164,7 +315,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::BN;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -177,7 +328,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         // +32 bytes (2 in the >>4 address field) per 16-wide K step;
                         // the first product of a tile overwrites the accumulator.
                         ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                         (kb | k) != 0 ? 1u : 0u);
+                                         (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     // release the stage to the producers once these MMAs have read it
                     if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
@@ -203,17 +354,28 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int ebuf = 0;
         for (int64_t u = cluster_idx; u < p.num_units; u += num_clusters, ++it) {
             int64_t tm, n0;
-            int nw;
-            work_unit(u, p, Cfg::BN, tm, n0, nw);
+            int nw, kb0, kb1;
+            work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
             const int chunks = nw / Cfg::EPI_COLS;
             const uint32_t buf = it & 1u;
             const uint32_t use = (it >> 1) & 1u;
-            if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns))
+            if (p.ksplit > 1) {
+                // all four epilogue warps decide together: they meet at named barriers
+                const bool ready = wait_phase(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
+                if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) break;
+            } else if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) {
                 break;
+            }
             ptx::tc_fence_after();
             const int64_t row0 = tm * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
             const bool rows_in = row0 < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
+            if (p.ksplit > 1) {
+                if (!split_k_epilogue<Cfg>(p, u, tm, n0, t_row, tempty_leader0, tempty_bar(buf), buf, q, lane,
+                                           threadIdx.x - 64, rank))
+                    break;
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t v[64];

@@ -21,6 +21,7 @@ enum WaitSite : uint32_t {
     kSiteMmaFull = 4,
     kSiteMmaDrain = 5,
     kSiteEpilogueTmemFull = 6,
+    kSiteSplitPieces = 7,
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t* status, uint32_t site) {
@@ -41,6 +42,27 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint32
             record_timeout(status, site);
             return false;
         }
+    }
+}
+
+// Wait until the global counter reaches `target` (other CTAs of the same
+// launch increment it), for at most `timeout_ns`.  Only used between CTAs that
+// are resident at the same time (the planner guarantees it).
+__device__ __forceinline__ bool wait_count(const uint32_t* addr, uint32_t target, uint32_t* status,
+                                           uint32_t site, uint64_t timeout_ns) {
+    uint64_t t0 = 0;
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+        if (v >= target) return true;
+        const uint64_t now = ptx::globaltimer_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > timeout_ns) {
+            record_timeout(status, site);
+            return false;
+        }
+        __nanosleep(64);
     }
 }
 

@@ -26,8 +26,8 @@
  *   - Argument errors are returned synchronously and nothing is enqueued.
  *   - The library uses the CUDA device that is current on the calling thread.
  *
- * Scratch memory.  The skinny (small-M, split-K) kernel keeps fp32 partial
- * sums and per-tile counters in a workspace the library allocates with
+ * Scratch memory.  The split-K kernels (small-M, and 2-CTA tiles with a
+ * split K loop) keep fp32 partial sums and per-tile counters in a workspace the library allocates with
  * cudaMalloc on the first call that needs it for a given (device, stream)
  * pair, grows when a larger problem needs more, and keeps until the process
  * exits.  Calls on the same stream are ordered and share that workspace
@@ -72,7 +72,11 @@ typedef enum {
     GEMM_VARIANT_TILE_2CTA_256x256 = 1, /* persistent, 2-CTA cluster, 256x256 tile per pair */
     GEMM_VARIANT_TILE_1CTA_128x128 = 2, /* persistent, one CTA per 128x128 tile */
     GEMM_VARIANT_TILE_1CTA_128x256 = 3, /* persistent, one CTA per 128x256 tile */
-    GEMM_VARIANT_SKINNY_SPLITK = 4      /* M <= 64: operands swapped, K split across all SMs */
+    GEMM_VARIANT_SKINNY_SPLITK = 4,     /* M <= 64: operands swapped, K split across all SMs */
+    GEMM_VARIANT_TILE_2CTA_SPLITK = 5   /* 2-CTA 256x256 tiles with each tile's K loop split over
+                                           several CTA pairs (for shapes with few tiles); falls
+                                           back to GEMM_VARIANT_TILE_2CTA_256x256 when the tiles
+                                           already fill the GPU */
 } gemm_variant_t;
 
 /*
@@ -96,7 +100,8 @@ GEMM_API gemm_status_t gemm_f16_nt(const void* A, const void* B, void* D,
  * gemm_f16_nt_variant -- gemm_f16_nt with the kernel chosen by the caller.
  * Same arguments and semantics; `variant` selects the kernel.  Returns
  * GEMM_ERR_INVALID_VALUE when the variant cannot run the shape (the skinny
- * variant needs M <= 64).  All variants compute the same D up to the order
+ * variant needs M <= 64).  The split-K variants keep fp32 partial sums in
+ * the per-stream workspace described above.  All variants compute the same D up to the order
  * of fp32 additions.
  */
 GEMM_API gemm_status_t gemm_f16_nt_variant(const void* A, const void* B, void* D,
@@ -134,6 +139,8 @@ typedef struct {
     int64_t num_full_tiles;  /* tiled: tiles run whole (the persistent grid's full rounds) */
     int32_t tail_split;      /* tiled: the other tiles are cut into this many column pieces */
     int32_t group_m;         /* tiled: tile rows per raster group (L2 reuse of A) */
+    int32_t k_split;         /* tiled split-K: pieces per tile's K loop (1 = none) */
+    int32_t reserved;
 } gemm_plan_t;
 
 /*

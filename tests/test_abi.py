@@ -123,8 +123,22 @@ def test_plans_for_the_named_workloads(lib):
     assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds + 4 tiles in quarters
     assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
     p = P(1024, 1024, 2048)
-    assert p["variant"] == "TILE_1CTA_128x256"                          # 32 tiles, cut in quarters
-    assert (p["num_full_tiles"], p["tail_split"], p["grid_ctas"]) == (0, 4, 128)
+    # 16 pair tiles but a short K loop (32 blocks): 128x256 tiles in quarters
+    assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1
+    p = P(512, 2048, 8192)
+    # 16 pair tiles fill less than half of the 76 pairs and K is long: each
+    # tile's K loop is split over 4 pairs (32 K blocks each), 64 units on 128 SMs
+    assert p["variant"] == "TILE_2CTA_SPLITK" and (p["k_split"], p["grid_ctas"]) == (4, 128)
+    assert p["workspace_bytes"] >= 16 * 4 * 256 * 256 * 4 + 16 * 4
+    p = P(1024, 1024, 2048, variant=g.Variant.TILE_2CTA_SPLITK)        # asked for explicitly: split
+    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
+    p = P(2048, 2048, 2048)
+    assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1    # 64 pair tiles: no split
+    p = P(1024, 4096, 4096)
+    assert p["variant"] == "TILE_1CTA_128x256"
+    # split-K asked for where the tiles already fill the GPU: plain pair tiles
+    p = P(8192, 8192, 8192, variant=g.Variant.TILE_2CTA_SPLITK)
+    assert p["variant"] == "TILE_2CTA_256x256" and p["k_split"] == 1
     p = P(128, 128, 64)
     assert p["variant"] == "TILE_1CTA_128x128" and p["k_blocks"] == 1
     assert (p["tail_split"], p["grid_ctas"]) == (2, 2)
@@ -135,7 +149,7 @@ def test_plans_for_the_named_workloads(lib):
     for v in g.Variant:
         if v in (g.Variant.AUTO,):
             continue
-        q = P(64, 256, 128, variant=v)
+        q = P(64, 256, 1024, variant=v)
         assert q["variant"] == v.name
         assert q["smem_bytes"] <= 232448
 
@@ -169,6 +183,19 @@ def test_tail_split_minimises_the_last_round(lib):
     # 128-wide tiles are cut at most in halves (pieces stay >= 64 columns)
     p = g.gemm_f16_nt_plan(128 * 153, 128, 64, g.Variant.TILE_1CTA_128x128, num_sms=152)
     assert (p["num_full_tiles"], p["tail_split"]) == (152, 2)
+
+
+def test_ksplit_choice(lib):
+    P = lambda *a, **k: g.gemm_f16_nt_plan(*a, num_sms=152, **k)  # noqa: E731
+    # pieces per tile: at most 8, every unit resident at once, >= 4 K blocks each
+    V = g.Variant.TILE_2CTA_SPLITK
+    assert P(256, 256, 64 * 64, variant=V)["k_split"] == 8
+    assert P(256, 256, 64 * 12, variant=V)["k_split"] == 3
+    assert P(256, 256, 64 * 7, variant=V)["k_split"] == 1                # under 4 K blocks per piece: no split
+    q = P(256 * 4, 256 * 5, 64 * 64, variant=V)                           # 20 tiles: 3 pieces fit on 76 pairs
+    assert q["k_split"] == 3 and q["grid_ctas"] == 2 * 20 * 3
+    # AUTO splits only long K loops (>= 40 K blocks)
+    assert P(256, 256, 64 * 39)["k_split"] == 1 and P(256, 256, 64 * 40)["k_split"] == 8
 
 
 def test_plan_errors(lib):
