@@ -43,6 +43,22 @@ class Variant(enum.IntEnum):
     TILE_2CTA_SPLITK = 5
 
 
+class Dtype(enum.IntEnum):
+    F16 = 0
+    BF16 = 1
+
+
+class Activation(enum.IntEnum):
+    NONE = 0
+    RELU = 1
+
+
+class Epilogue(ctypes.Structure):
+    """Mirror of gemm_epilogue_t: D = act(alpha * (A Bᵀ) + beta * C + bias[n])."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("C", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class LibraryMissing(RuntimeError):
     """The compiled CUDA library is not there (build it first)."""
 
@@ -94,6 +110,10 @@ def load():
         lib.gemm_f16_nt_plan.restype = ctypes.c_int
         lib.gemm_f16_nt_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
         lib.gemm_f16_nt_noalloc.restype = ctypes.c_int
+        lib.gemm_bf16_nt.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.gemm_bf16_nt.restype = ctypes.c_int
+        lib.gemm_nt_ex.argtypes = [ctypes.c_int, p, p, p, i64, i64, i64, ctypes.POINTER(Epilogue), ctypes.c_int, p]
+        lib.gemm_nt_ex.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -118,15 +138,16 @@ def _stream_handle(stream, device=None) -> int | None:
     return int(stream) or None
 
 
-def _operands(A, B, D, M, N, K):
+def _operands(A, B, D, M, N, K, dtype=None):
     """(a_ptr, b_ptr, d_ptr, M, N, K, device) from tensors or raw pointers."""
     if _is_tensor(A):
         import torch
+        want = torch.bfloat16 if dtype == Dtype.BF16 else torch.float16
         for name, t in (("A", A), ("B", B), ("D", D)):
             if not _is_tensor(t):
                 raise TypeError(f"{name}: mix of tensors and raw pointers")
-            if t.dtype != torch.float16:
-                raise TypeError(f"{name} must be torch.float16, got {t.dtype}")
+            if t.dtype != want:
+                raise TypeError(f"{name} must be {want}, got {t.dtype}")
             if not t.is_cuda:
                 raise ValueError(f"{name} must be a CUDA tensor")
             if t.dim() != 2 or not t.is_contiguous():
@@ -184,6 +205,36 @@ def gemm_f16_nt_noalloc(A, B, D, M=None, N=None, K=None, stream=None) -> None:
     """
     a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K)
     _call("gemm_f16_nt_noalloc", (a or None, b or None, d or None, m, n, k, _stream_handle(stream, dev)), dev)
+
+
+def gemm_bf16_nt(A, B, D, M=None, N=None, K=None, stream=None) -> None:
+    """D = A·Bᵀ for bf16 tensors (fp32 accumulation, bf16 output); asynchronous."""
+    a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K, Dtype.BF16)
+    _call("gemm_bf16_nt", (a or None, b or None, d or None, m, n, k, _stream_handle(stream, dev)), dev)
+
+
+def _tensor_dtype(A):
+    import torch
+    return Dtype.BF16 if getattr(A, "dtype", None) == torch.bfloat16 else Dtype.F16
+
+
+def gemm_nt_ex(A, B, D, M=None, N=None, K=None, dtype=None, alpha=1.0, beta=0.0, C=None, bias=None,
+               activation=Activation.NONE, variant=Variant.AUTO, stream=None) -> None:
+    """D = act(alpha·A·Bᵀ + beta·C + bias[n]) for fp16 or bf16 (dtype taken from the tensors)."""
+    if dtype is None:
+        dtype = _tensor_dtype(A) if _is_tensor(A) else Dtype.F16
+    a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K, Dtype(dtype))
+    def ptr(x):
+        if x is None:
+            return None
+        if _is_tensor(x):
+            if x.dtype != D.dtype or not x.is_contiguous():
+                raise TypeError("C and bias must be contiguous and of D's dtype")
+            return x.data_ptr()
+        return int(x)
+    epi = Epilogue(float(alpha), float(beta), ptr(C), ptr(bias), int(activation), 0)
+    _call("gemm_nt_ex", (int(dtype), a or None, b or None, d or None, m, n, k, ctypes.byref(epi), int(variant),
+                         _stream_handle(stream, dev)), dev)
 
 
 def gemm_f16_nt_check(stream=None, device=None) -> None:

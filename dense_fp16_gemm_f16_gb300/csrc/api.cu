@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -13,6 +14,7 @@
 #include <utility>
 
 #include "config.h"
+#include "epilogue.cuh"
 #include "gemm_f16.h"
 #include "launch.h"
 
@@ -128,7 +130,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
 
     if (variant == GEMM_VARIANT_SKINNY_SPLITK) {
         const int mn = skinny_mn(M);
-        const SkinnyOps& ops = skinny_ops(mn);
+        const SkinnyOps& ops = skinny_ops(mn, 0);
         pl->cta_group = 1;
         pl->tile_m = mn;
         pl->tile_n = 128;
@@ -157,9 +159,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
         variant = GEMM_VARIANT_TILE_2CTA_256x256;   // enough tiles already: no split
     pl->variant = variant;
     const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK;
-    const TiledOps& ops = (variant == GEMM_VARIANT_TILE_2CTA_256x256 || ksplit_variant) ? tiled_ops_2cta256()
-                          : variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
-                                                                      : tiled_ops_1cta256();
+    const TiledOps& ops = (variant == GEMM_VARIANT_TILE_2CTA_256x256 || ksplit_variant) ? tiled_ops_2cta256(0)
+                          : variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128(0)
+                                                                      : tiled_ops_1cta256(0);
     pl->cta_group = ops.cta_group;
     pl->tile_m = ops.tile_m;
     pl->tile_n = ops.tile_n;
@@ -238,11 +240,14 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
-        const TiledOps* tiled[3] = {&tiled_ops_2cta256(), &tiled_ops_1cta128(), &tiled_ops_1cta256()};
-        for (const TiledOps* t : tiled)
-            if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
-        for (int mn : {16, 32, 64})
-            if (skinny_ops(mn).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+        const TiledOps* tiled[3] = {&tiled_ops_2cta256(0), &tiled_ops_1cta128(0), &tiled_ops_1cta256(0)};
+        for (int dt : {0, 1}) {
+            const TiledOps* all[3] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt)};
+            for (const TiledOps* t : all)
+                if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+            for (int mn : {16, 32, 64})
+                if (skinny_ops(mn, dt).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+        }
         int clusters = 0, per128 = 0, per256 = 0;
         if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
             tiled[2]->max_active(&per256) != cudaSuccess) {
@@ -268,12 +273,12 @@ Limits limits_of(const DeviceState& d) {
 // 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
 // box of box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
 bool encode_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, uint32_t box_inner,
-               uint32_t box_outer) {
+               uint32_t box_outer, int dtype = 0) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+    const CUresult r = g_encode(map, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
                                 strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -335,11 +340,56 @@ uint64_t timeout_for(int64_t k_blocks) {
     return 2000000000ull + static_cast<uint64_t>(k_blocks) * 2000ull;
 }
 
+// Elementwise D = act(beta * C + bias) for K == 0 (the empty sum) when a fused
+// epilogue is asked for.
+template <class T>
+__global__ void epilogue_only_kernel(T* D, int64_t M, int64_t N, EpiParams e) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / N, col = i - (i / N) * N;
+        D[i] = Elem<T>::from_float(epi_apply1<T>(e, 0.0f, row, col, N));
+    }
+}
+
+EpiParams epi_params(const gemm_epilogue_t* e) {
+    EpiParams p;
+    p.alpha = 1.0f;
+    p.beta = 0.0f;
+    p.C = nullptr;
+    p.bias = nullptr;
+    p.act = 0;
+    p.on = 0;
+    if (e == nullptr) return p;
+    p.alpha = e->alpha;
+    p.beta = e->beta;
+    p.C = e->beta != 0.0f ? e->C : nullptr;
+    p.bias = e->bias;
+    p.act = e->activation;
+    p.on = (p.alpha != 1.0f || p.C != nullptr || p.bias != nullptr || p.act != 0) ? 1 : 0;
+    return p;
+}
+
 gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-                  gemm_variant_t variant, gemm_stream_t stream) {
+                  gemm_variant_t variant, gemm_stream_t stream, int dtype = 0,
+                  const gemm_epilogue_t* epilogue = nullptr) {
     // ---- host-only argument checks (nothing touches a device before these pass)
     gemm_status_t st = check_sizes(M, N, K);
     if (st != GEMM_OK) return st;
+    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_VALUE;
+    const EpiParams epi = epi_params(epilogue);
+    if (epilogue != nullptr) {
+        if (epilogue->activation != GEMM_ACT_NONE && epilogue->activation != GEMM_ACT_RELU)
+            return GEMM_ERR_INVALID_VALUE;
+        if (epilogue->beta != 0.0f && epilogue->C == nullptr) return GEMM_ERR_INVALID_VALUE;
+        if ((epi.C && !aligned16(epi.C)) || (epi.bias && !aligned16(epi.bias))) return GEMM_ERR_MISALIGNED;
+        // C may be D itself (an in-place update); it may not partly overlap D, and
+        // the bias may not overlap D at all
+        if (M > 0 && N > 0) {
+            if (epi.C && epi.C != D && ranges_overlap(epi.C, M * N * 2, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
+            if (epi.bias && ranges_overlap(epi.bias, N * 2, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
+        }
+    }
     if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -357,6 +407,15 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (K == 0) {  // the empty sum
+        if (epi.on) {
+            const int blocks = static_cast<int>(std::min<int64_t>(cdiv(M * N, 256), 8 * dev->sms));
+            if (dtype == GEMM_DTYPE_BF16)
+                epilogue_only_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(D), M, N, epi);
+            else
+                epilogue_only_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<__half*>(D), M, N, epi);
+            if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+            return GEMM_OK;
+        }
         if (cudaMemsetAsync(D, 0, static_cast<size_t>(d_bytes), s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
@@ -369,9 +428,10 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     if (st != GEMM_OK) return st;
 
     if (pl.variant == GEMM_VARIANT_SKINNY_SPLITK) {
-        const SkinnyOps& ops = skinny_ops(pl.tile_m);
+        const SkinnyOps& ops = skinny_ops(pl.tile_m, dtype);
         CUtensorMap tw, tx;
-        if (!encode_2d(&tw, B, K, N, kBK, 128) || !encode_2d(&tx, A, K, M, kBK, static_cast<uint32_t>(ops.mn)))
+        if (!encode_2d(&tw, B, K, N, kBK, 128, dtype) ||
+            !encode_2d(&tx, A, K, M, kBK, static_cast<uint32_t>(ops.mn), dtype))
             return GEMM_ERR_INVALID_VALUE;
         Workspace* ws = nullptr;
         const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
@@ -389,6 +449,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         p.partials = ws->partials;
         p.counters = ws->counters;
         p.D = D;
+        p.epi = epi;
         p.status = dev->status;
         p.timeout_ns = timeout_for(pl.k_blocks);
         if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
@@ -399,9 +460,9 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     }
 
     const TiledOps& ops = (pl.variant == GEMM_VARIANT_TILE_2CTA_256x256 || pl.variant == GEMM_VARIANT_TILE_2CTA_SPLITK)
-                              ? tiled_ops_2cta256()
-                          : pl.variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128()
-                                                                         : tiled_ops_1cta256();
+                              ? tiled_ops_2cta256(dtype)
+                          : pl.variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128(dtype)
+                                                                         : tiled_ops_1cta256(dtype);
     Workspace* ws = nullptr;
     if (pl.k_split > 1) {
         const size_t partial_bytes = static_cast<size_t>(pl.m_tiles * pl.n_tiles) * pl.k_split * ops.tile_m *
@@ -411,9 +472,9 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     }
     CUtensorMap ta, tb, tbp, td;
     const uint32_t b_rows = static_cast<uint32_t>(ops.tile_n / ops.cta_group);
-    if (!encode_2d(&ta, A, K, M, kBK, 128) || !encode_2d(&tb, B, K, N, kBK, b_rows) ||
-        !encode_2d(&tbp, B, K, N, kBK, b_rows / static_cast<uint32_t>(pl.tail_split)) ||
-        !encode_2d(&td, D, N, M, 64, 32))
+    if (!encode_2d(&ta, A, K, M, kBK, 128, dtype) || !encode_2d(&tb, B, K, N, kBK, b_rows, dtype) ||
+        !encode_2d(&tbp, B, K, N, kBK, b_rows / static_cast<uint32_t>(pl.tail_split), dtype) ||
+        !encode_2d(&td, D, N, M, 64, 32, dtype))
         return GEMM_ERR_INVALID_VALUE;
     TiledParams p;
     p.M = static_cast<int32_t>(M);
@@ -432,6 +493,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.partials = ws ? ws->partials : nullptr;
     p.counters = ws ? ws->counters : nullptr;
     p.D = D;
+    p.epi = epi;
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
     if (ops.launch(ta, tb, tbp, td, p, pl.grid_ctas, s) != cudaSuccess) {
@@ -497,7 +559,7 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
     gemm_plan_t pl;
     st = make_plan(M, N, K, GEMM_VARIANT_SKINNY_SPLITK, limits_of(*dev), &pl);
     if (st != GEMM_OK) return st;
-    const SkinnyOps& ops = skinny_ops(pl.tile_m);
+    const SkinnyOps& ops = skinny_ops(pl.tile_m, 0);
     const size_t counter_bytes = static_cast<size_t>(round_up(pl.n_tiles * 4, 256));
     const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
     if (counter_bytes + partial_bytes > static_cast<size_t>(GEMM_F16_NOALLOC_SCRATCH_BYTES))
@@ -528,6 +590,7 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
     p.partials = reinterpret_cast<float*>(scratch + counter_bytes);
     p.counters = reinterpret_cast<uint32_t*>(scratch);
     p.D = D;
+    p.epi = epi_params(nullptr);
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
     if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
@@ -549,6 +612,17 @@ GEMM_API gemm_status_t gemm_f16_nt(const void* A, const void* B, void* D, int64_
 GEMM_API gemm_status_t gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N,
                                            int64_t K, gemm_variant_t variant, gemm_stream_t stream) {
     return run(A, B, D, M, N, K, variant, stream);
+}
+
+GEMM_API gemm_status_t gemm_bf16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                                    gemm_stream_t stream) {
+    return run(A, B, D, M, N, K, GEMM_VARIANT_AUTO, stream, GEMM_DTYPE_BF16, nullptr);
+}
+
+GEMM_API gemm_status_t gemm_nt_ex(gemm_dtype_t dtype, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                  int64_t K, const gemm_epilogue_t* epilogue, gemm_variant_t variant,
+                                  gemm_stream_t stream) {
+    return run(A, B, D, M, N, K, variant, stream, static_cast<int>(dtype), epilogue);
 }
 
 GEMM_API gemm_status_t gemm_f16_nt_check(gemm_stream_t stream) {

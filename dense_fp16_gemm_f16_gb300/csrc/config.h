@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 #if defined(__CUDACC__)
@@ -60,7 +61,6 @@ struct TiledConfig {
     static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;  // + slack to align the base
-    static constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
     static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT) % 1024 == 0, "stage tiles must stay 1024-aligned");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 up to 256");
     static_assert(B_ROWS <= 256, "TMA box rows are limited to 256");
@@ -84,7 +84,9 @@ struct TiledParams {
     int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces (split-K)
     float* partials;          // split-K: [num_tiles][ksplit][BM][BN] fp32
     uint32_t* counters;       // split-K: [num_tiles], zero between calls
-    void* D;                  // split-K: the output, written by the slice reductions
+    void* D;                  // the output (fp16 or bf16 [M][N]); written directly by the
+                              // split-K slice reductions, through tmD otherwise
+    EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
     uint32_t* status;         // device status word (0 = ok)
     uint64_t timeout_ns;      // per-wait budget
 };
@@ -200,7 +202,6 @@ struct SkinnyConfig {
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
-    static constexpr uint32_t IDESC = ptx::idesc_f16_f32(128, MN);
     static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
@@ -219,7 +220,8 @@ struct SkinnyParams {
     int64_t units;            // n_tiles * k_blocks
     float* partials;          // [G][max_tiles_per_cta][MN][128] fp32
     uint32_t* counters;       // [n_tiles], zero between calls
-    void* D;                  // __half [M][N]
+    void* D;                  // fp16 or bf16 [M][N]
+    EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
     uint32_t* status;
     uint64_t timeout_ns;
 };

@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "config.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "wait.cuh"
 
@@ -38,7 +39,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[MN]) 
     }
 }
 
-template <class Cfg>
+template <class Cfg, class T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const SkinnyParams p) {
@@ -89,6 +90,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
+    constexpr uint32_t idesc = ptx::idesc_kind_f16(128, MN, Elem<T>::kFormat);
     const int64_t G = p.num_ctas;
     const int64_t W = p.units;
     const int64_t KB = p.k_blocks;
@@ -148,7 +150,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint64_t x_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
-                        ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, Cfg::IDESC,
+                        ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
                                         (u != seg_start || k != 0) ? 1u : 0u);
                     ptx::mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -164,7 +166,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int q = warp & 3;
         const int r = q * 32 + lane;                     // row of the 128-row tile = output column
         const int etid = threadIdx.x - 64;               // 0..127 among the epilogue threads
-        __half* D = static_cast<__half*>(p.D);
+        T* D = static_cast<T*>(p.D);
         const int64_t first_tile = u0 / KB;
         uint32_t seg = 0;
         for (int64_t u = u0; u < u1; ++seg) {
@@ -191,8 +193,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 // the whole K loop of this tile ran here
                 if (n < p.N) {
 #pragma unroll
-                    for (int m = 0; m < MN; ++m)
-                        if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(__uint_as_float(v[m]));
+                    for (int m = 0; m < MN; ++m) {
+                        if (m < p.M) {
+                            float x = __uint_as_float(v[m]);
+                            if (p.epi.on) x = epi_apply1<T>(p.epi, x, m, n, p.N);
+                            D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
+                        }
+                    }
                 }
             } else {
                 // The piece holding k = 0 ends the range of the CTA before the
@@ -255,8 +262,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                                 }
                         }
 #pragma unroll
-                        for (int m = 0; m < MN; ++m)
-                            if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = __float2half_rn(acc[m]);
+                        for (int m = 0; m < MN; ++m) {
+                            if (m < p.M) {
+                                const float x = p.epi.on ? epi_apply1<T>(p.epi, acc[m], m, n, p.N) : acc[m];
+                                D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
+                            }
+                        }
                     }
                     if (etid == 0) p.counters[t] = 0u;  // re-armed for the next call on this stream
                 }

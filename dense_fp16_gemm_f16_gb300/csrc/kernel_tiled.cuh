@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "config.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "wait.cuh"
 
@@ -45,13 +46,13 @@ __device__ __forceinline__ int64_t split_quad_offset(int col, int row) {
 // multiple of 8 wide), pieces in ascending order, written to D as fp16.
 // Loads go out in batches of up to 8 float4 (two 8-column groups when S = 2,
 // else one group with up to 4 pieces) before the additions that use them.
-template <class Cfg, int S>
+template <class Cfg, class T, int S>
 __device__ __forceinline__ void split_k_reduce_row(const float* base, int r_local, int c_begin, int c_end,
                                                    int64_t n0, int64_t grow, const TiledParams& p) {
     constexpr int GB = (S <= 2) ? 2 : 1;            // 8-column groups per batch
     constexpr int JC = (S < 4) ? S : 4;             // pieces per batch
     const int64_t piece_stride = static_cast<int64_t>(Cfg::BM) * Cfg::BN;
-    __half* D = static_cast<__half*>(p.D);
+    T* D = static_cast<T*>(p.D);
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 8 * GB) {
         float acc[GB][8];
@@ -92,12 +93,10 @@ __device__ __forceinline__ void split_k_reduce_row(const float* base, int r_loca
             const int cg = c + 8 * g;
             const int64_t gcol = n0 + cg;
             if (cg < c_end && gcol < p.N) {         // N % 8 == 0: groups are all in or all out
+                if (p.epi.on) epi_apply8<T>(p.epi, acc[g], grow, gcol, p.M, p.N);
                 uint32_t h[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __half2 x = __floats2half2_rn(acc[g][2 * e], acc[g][2 * e + 1]);
-                    h[e] = *reinterpret_cast<const uint32_t*>(&x);
-                }
+                for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(acc[g][2 * e], acc[g][2 * e + 1]);
                 *reinterpret_cast<uint4*>(D + grow * static_cast<int64_t>(p.N) + gcol) =
                     make_uint4(h[0], h[1], h[2], h[3]);
             }
@@ -111,7 +110,7 @@ __device__ __forceinline__ void split_k_reduce_row(const float* base, int r_loca
 // this CTA's rows over the unit's 1/ksplit slice of columns -- pieces in
 // ascending order, so the result does not depend on timing -- and store that
 // slice of D.  The last CTA through re-arms the tile's counter.
-template <class Cfg>
+template <class Cfg, class T>
 __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u, int64_t tm, int64_t n0,
                                                  uint32_t t_row, uint32_t tempty_leader0, uint32_t tempty_local,
                                                  uint32_t buf, int q, int lane, int etid, uint32_t rank) {
@@ -165,13 +164,13 @@ __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u
     if (grow < p.M) {
         const float* base = p.partials + t * S * static_cast<int64_t>(BN) * Cfg::BM;
         switch (S) {
-            case 2: split_k_reduce_row<Cfg, 2>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 3: split_k_reduce_row<Cfg, 3>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 4: split_k_reduce_row<Cfg, 4>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 5: split_k_reduce_row<Cfg, 5>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 6: split_k_reduce_row<Cfg, 6>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 7: split_k_reduce_row<Cfg, 7>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            default: split_k_reduce_row<Cfg, 8>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 2: split_k_reduce_row<Cfg, T, 2>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 3: split_k_reduce_row<Cfg, T, 3>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 4: split_k_reduce_row<Cfg, T, 4>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 5: split_k_reduce_row<Cfg, T, 5>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 6: split_k_reduce_row<Cfg, T, 6>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            case 7: split_k_reduce_row<Cfg, T, 7>(base, r_local, c_begin, c_end, n0, grow, p); break;
+            default: split_k_reduce_row<Cfg, T, 8>(base, r_local, c_begin, c_end, n0, grow, p); break;
         }
     }
     // 4. the last of the 2 * S * CG arrivals re-arms the counter for the next call
@@ -183,7 +182,7 @@ __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u
     return true;
 }
 
-template <class Cfg>
+template <class Cfg, class T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBpiece, const __grid_constant__ CUtensorMap tmD,
@@ -305,7 +304,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 int64_t tm, n0;
                 int nw, kb0, kb1;
                 work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
-                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::BM, nw);
+                const uint32_t idesc = ptx::idesc_kind_f16(Cfg::BM, nw, Elem<T>::kFormat);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
                 // the epilogue must have drained this accumulator buffer
@@ -371,7 +370,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool rows_in = row0 < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
             if (p.ksplit > 1) {
-                if (!split_k_epilogue<Cfg>(p, u, tm, n0, t_row, tempty_leader0, tempty_bar(buf), buf, q, lane,
+                if (!split_k_epilogue<Cfg, T>(p, u, tm, n0, t_row, tempty_leader0, tempty_bar(buf), buf, q, lane,
                                            threadIdx.x - 64, rank))
                     break;
                 continue;
@@ -403,13 +402,14 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     uint8_t* row_ptr = sb + lane * (Cfg::EPI_COLS * 2);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * j + e]);
+                        if (p.epi.on && col0 + 8 * j < p.N)
+                            epi_apply8<T>(p.epi, x, row0 + lane, col0 + 8 * j, p.M, p.N);
                         uint32_t h[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __half2 x = __floats2half2_rn(__uint_as_float(v[8 * j + 2 * e]),
-                                                                __uint_as_float(v[8 * j + 2 * e + 1]));
-                            h[e] = *reinterpret_cast<const uint32_t*>(&x);
-                        }
+                        for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(x[2 * e], x[2 * e + 1]);
                         *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) << 4)) =
                             make_uint4(h[0], h[1], h[2], h[3]);
                     }

@@ -29,9 +29,10 @@ struct SkinnyOps {
                           int grid_ctas, cudaStream_t stream);
 };
 
-const TiledOps& tiled_ops_2cta256();
-const TiledOps& tiled_ops_1cta128();
-const TiledOps& tiled_ops_1cta256();
-const SkinnyOps& skinny_ops(int mn);  // mn = 16, 32 or 64
+// dtype: 0 = fp16 operands and output, 1 = bf16
+const TiledOps& tiled_ops_2cta256(int dtype);
+const TiledOps& tiled_ops_1cta128(int dtype);
+const TiledOps& tiled_ops_1cta256(int dtype);
+const SkinnyOps& skinny_ops(int mn, int dtype);  // mn = 16, 32 or 64
 
 }  // namespace gemm_gb300

@@ -6,10 +6,10 @@
 
 namespace gemm_gb300 {
 
-template <class Cfg>
+template <class Cfg, class T>
 struct TiledLauncher {
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg::SMEM_BYTES);
     }
 
@@ -26,9 +26,9 @@ struct TiledLauncher {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg>, &cfg);
+            return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg, T>, &cfg);
         } else {
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg>, kThreads,
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg, T>, kThreads,
                                                                  Cfg::SMEM_BYTES);
         }
     }
@@ -55,7 +55,7 @@ struct TiledLauncher {
             cfg.numAttrs = 2;
         }
         cfg.attrs = attr;
-        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg>, a, b, b_piece, d, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T>, a, b, b_piece, d, p);
     }
 
     static const TiledOps& ops() {

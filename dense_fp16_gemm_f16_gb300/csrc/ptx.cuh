@@ -297,14 +297,15 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16: fp16 A and B, both
-// K-major, fp32 accumulator, no negation, dense.  M is the MMA's full M (the
-// pair's M for cta_group::2), N its N.
-//   bits  4-5   D format (1 = f32)      bits  7-9  A format (0 = f16)
-//   bits 10-12  B format (0 = f16)      bit  15/16 A/B major (0 = K-major)
+// Instruction descriptor for tcgen05.mma kind::f16: A and B both fp16
+// (format 0) or both bf16 (format 1), both K-major, fp32 accumulator, no
+// negation, dense.  M is the MMA's full M (the pair's M for cta_group::2),
+// N its N.
+//   bits  4-5   D format (1 = f32)      bits  7-9  A format (0 = f16, 1 = bf16)
+//   bits 10-12  B format (same as A)    bit  15/16 A/B major (0 = K-major)
 //   bits 17-22  N >> 3                  bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-    return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_format) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (0u << 15) | (0u << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 

@@ -2,6 +2,10 @@
 #include "launch_tiled.cuh"
 
 namespace gemm_gb300 {
-const TiledOps& tiled_ops_1cta128() { return TiledLauncher<Cfg1cta128>::ops(); }
-const TiledOps& tiled_ops_1cta256() { return TiledLauncher<Cfg1cta256>::ops(); }
+const TiledOps& tiled_ops_1cta128(int dtype) {
+    return dtype == 1 ? TiledLauncher<Cfg1cta128, __nv_bfloat16>::ops() : TiledLauncher<Cfg1cta128, __half>::ops();
+}
+const TiledOps& tiled_ops_1cta256(int dtype) {
+    return dtype == 1 ? TiledLauncher<Cfg1cta256, __nv_bfloat16>::ops() : TiledLauncher<Cfg1cta256, __half>::ops();
+}
 }  // namespace gemm_gb300

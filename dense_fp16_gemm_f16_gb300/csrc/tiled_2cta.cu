@@ -2,5 +2,7 @@
 #include "launch_tiled.cuh"
 
 namespace gemm_gb300 {
-const TiledOps& tiled_ops_2cta256() { return TiledLauncher<Cfg2cta256>::ops(); }
+const TiledOps& tiled_ops_2cta256(int dtype) {
+    return dtype == 1 ? TiledLauncher<Cfg2cta256, __nv_bfloat16>::ops() : TiledLauncher<Cfg2cta256, __half>::ops();
+}
 }  // namespace gemm_gb300

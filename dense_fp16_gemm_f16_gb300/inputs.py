@@ -135,3 +135,28 @@ def sample_entries(M: int, N: int, seed: int, n_rows: int = 8, n_cols: int = 8,
     r_parts.append(np.array([0, 0, M - 1, M - 1], dtype=np.int64))
     c_parts.append(np.array([0, N - 1, 0, N - 1], dtype=np.int64))
     return np.concatenate(r_parts), np.concatenate(c_parts)
+
+
+def draw_bf16(rows: int, cols: int, dist: str, seed: int, K: int | None = None) -> np.ndarray:
+    """bf16 operands as uint16 bit patterns: the same float64 draws as ``draw``,
+    rounded to float32 and then to bf16 by torch (nearest, ties to even).  Any
+    bf16 value is a valid input; the CPU oracle and the GPU see the same bits."""
+    import torch
+
+    K = cols if K is None else K
+    rng = np.random.default_rng(seed)
+    n = rows * cols
+    if dist == "uniform":
+        x = rng.uniform(-1.0, 1.0, n)
+    elif dist.startswith("normal:"):
+        x = rng.normal(0.0, _sigma(dist, K), n)
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).reshape(rows, cols).copy()
+
+
+def operands_bf16(M: int, N: int, K: int, dist_a: str = "uniform", dist_b: str = "uniform",
+                  seed: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """(A [M,K], B [N,K]) bf16 bit patterns, A from ``seed`` and B from ``seed + 1000``."""
+    return draw_bf16(M, K, dist_a, seed, K=K), draw_bf16(N, K, dist_b, seed + 1000, K=K)

@@ -79,6 +79,40 @@ typedef enum {
                                            already fill the GPU */
 } gemm_variant_t;
 
+/* Element type of A, B, D (and C, bias): both operands share it (the MMA
+ * multiplies f16 by f16 or bf16 by bf16, accumulating in fp32). */
+typedef enum {
+    GEMM_DTYPE_F16 = 0,
+    GEMM_DTYPE_BF16 = 1
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1
+} gemm_activation_t;
+
+/*
+ * Fused output transform, applied in fp32 to the fp32 accumulator before the
+ * single rounding of D:   D = act(alpha * (A B^T) + beta * C + bias[n])
+ * (the scaled update C = alpha A B + beta C and the bias/activation fusion of
+ * the GEMM blog post, sections 2.1 and 5.4).
+ *   alpha       scale of A B^T
+ *   beta        scale of C; 0 means C is not read
+ *   C           [M][N] row-major, same dtype as D, 16-byte aligned; may be D
+ *               itself (in-place update) but may not partly overlap it;
+ *               required when beta != 0
+ *   bias        [N], same dtype, 16-byte aligned, added to every row; NULL = none
+ *   activation  a gemm_activation_t, applied last
+ */
+typedef struct {
+    float alpha;
+    float beta;
+    const void* C;
+    const void* bias;
+    int32_t activation;
+    int32_t reserved;
+} gemm_epilogue_t;
+
 /*
  * gemm_f16_nt -- D = A * B^T, the operation above.
  *
@@ -106,6 +140,28 @@ GEMM_API gemm_status_t gemm_f16_nt(const void* A, const void* B, void* D,
  */
 GEMM_API gemm_status_t gemm_f16_nt_variant(const void* A, const void* B, void* D,
                                   int64_t M, int64_t N, int64_t K,
+                                  gemm_variant_t variant, gemm_stream_t stream);
+
+/*
+ * gemm_bf16_nt -- the same operation for bf16 A, B and D (fp32 accumulation,
+ * D rounded to nearest even).  The pages list bf16 beside fp16 (the GEMM blog
+ * post, section 2.2: same storage size, fp32's exponent range).  Arguments,
+ * layout, ownership and errors as for gemm_f16_nt.
+ */
+GEMM_API gemm_status_t gemm_bf16_nt(const void* A, const void* B, void* D,
+                                    int64_t M, int64_t N, int64_t K, gemm_stream_t stream);
+
+/*
+ * gemm_nt_ex -- the general entry point: element type, an optional fused
+ * epilogue (NULL = plain D = A B^T) and the kernel variant (GEMM_VARIANT_AUTO
+ * to let the planner choose).  Arguments otherwise as for gemm_f16_nt.
+ * Additional errors: GEMM_ERR_INVALID_VALUE for an unknown dtype or
+ * activation, beta != 0 with C == NULL, C partly overlapping D, or bias
+ * overlapping D; GEMM_ERR_MISALIGNED for C or bias not 16-byte aligned.
+ * With K == 0 the result is act(beta * C + bias) (the empty sum is zero).
+ */
+GEMM_API gemm_status_t gemm_nt_ex(gemm_dtype_t dtype, const void* A, const void* B, void* D,
+                                  int64_t M, int64_t N, int64_t K, const gemm_epilogue_t* epilogue,
                                   gemm_variant_t variant, gemm_stream_t stream);
 
 /*

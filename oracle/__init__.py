@@ -92,6 +92,14 @@ class Oracle:
         lib.oracle_gemm_nt_entries.restype = ctypes.c_int
         lib.oracle_gemm_nt_rows.argtypes = [p, p, i64, i64, i64, i64, i64, p, p, ctypes.c_int]
         lib.oracle_gemm_nt_rows.restype = ctypes.c_int
+        lib.oracle_bf16_to_f64.argtypes = [p, p, i64]
+        lib.oracle_bf16_to_f64.restype = None
+        lib.oracle_f64_to_bf16.argtypes = [p, p, i64]
+        lib.oracle_f64_to_bf16.restype = None
+        d = ctypes.c_double
+        lib.oracle_gemm_nt_ex.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p, i64, i64, i64,
+                                          d, d, p, p, ctypes.c_int, p, p, ctypes.c_int]
+        lib.oracle_gemm_nt_ex.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -111,6 +119,20 @@ class Oracle:
         out = np.empty(a.shape, dtype=np.uint16)
         self.lib.oracle_f64_to_f16(_ptr(a), _ptr(out), a.size)
         return out.view(np.float16)
+
+    def bf16_to_f64(self, bits) -> np.ndarray:
+        """Decode bf16 bit patterns (uint16) into float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_bf16_to_f64(_ptr(b), _ptr(out), b.size)
+        return out
+
+    def f64_to_bf16(self, x) -> np.ndarray:
+        """Round float64 values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+        a = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(a.shape, dtype=np.uint16)
+        self.lib.oracle_f64_to_bf16(_ptr(a), _ptr(out), a.size)
+        return out
 
     # -- the GEMM -------------------------------------------------------------
     @staticmethod
@@ -190,3 +212,80 @@ def gemm_rows(A, B, row_begin, row_end, nthreads=None, want_sums=False):
 
 def gemm(A, B, nthreads=None, want_sums=False):
     return default().gemm(A, B, nthreads=nthreads, want_sums=want_sums)
+
+
+# ---------------------------------------------------------------------------
+# element type + fused epilogue:  D = round(act(alpha * A Bᵀ + beta * C + bias[n]))
+# ---------------------------------------------------------------------------
+DTYPES = {"f16": 0, "bf16": 1}
+
+
+def _bits(x, dtype: str) -> np.ndarray:
+    """uint16 bit patterns of an operand: float16 arrays for f16, uint16 for bf16."""
+    a = np.ascontiguousarray(x)
+    if dtype == "f16":
+        if a.dtype != np.float16:
+            raise TypeError(f"f16 operands must be float16 arrays, got {a.dtype}")
+        return a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 operands must be uint16 bit-pattern arrays, got {a.dtype}")
+    return a
+
+
+def _gemm_ex(o: Oracle, A, B, dtype, alpha, beta, C, bias, relu, rows=None, cols=None,
+             row_begin=0, row_end=None, nthreads=None, want_pre=False):
+    if dtype not in DTYPES:
+        raise ValueError(f"dtype must be one of {sorted(DTYPES)}")
+    Ab, Bb = _bits(A, dtype), _bits(B, dtype)
+    if Ab.ndim != 2 or Bb.ndim != 2 or Ab.shape[1] != Bb.shape[1]:
+        raise ValueError("need A [M,K] and B [N,K]")
+    M, K = Ab.shape
+    N = Bb.shape[0]
+    Cb = None if C is None or beta == 0 else _bits(C, dtype)
+    if Cb is not None and Cb.shape != (M, N):
+        raise ValueError("C must be [M, N]")
+    biasb = None if bias is None else _bits(bias, dtype)
+    if biasb is not None and biasb.shape != (N,):
+        raise ValueError("bias must be [N]")
+    if rows is not None:
+        r = np.ascontiguousarray(rows, dtype=np.int64).ravel()
+        c = np.ascontiguousarray(cols, dtype=np.int64).ravel()
+        shape, count = r.shape, r.size
+        rp, cp = _ptr(r), _ptr(c)
+        rb, re = 0, 0
+    else:
+        row_end = M if row_end is None else row_end
+        shape, count = (row_end - row_begin, N), 0
+        rp = cp = None
+        rb, re = row_begin, row_end
+    out = np.empty(shape, dtype=np.uint16)
+    pre = np.empty(shape, dtype=np.float64) if want_pre else None
+    rc = o.lib.oracle_gemm_nt_ex(DTYPES[dtype], _ptr(Ab), _ptr(Bb), M, N, K, rp, cp, count, rb, re,
+                                 float(alpha), float(beta), _ptr(Cb), _ptr(biasb), 1 if relu else 0,
+                                 _ptr(pre), _ptr(out), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_gemm_nt_ex rejected its arguments")
+    res = out.view(np.float16) if dtype == "f16" else out
+    return (res, pre) if want_pre else res
+
+
+def gemm_ex(A, B, dtype="f16", alpha=1.0, beta=0.0, C=None, bias=None, relu=False,
+            nthreads=None, want_pre=False, oracle=None):
+    """Whole D (float16 for f16, uint16 bf16 bit patterns for bf16)."""
+    return _gemm_ex(oracle or default(), A, B, dtype, alpha, beta, C, bias, relu,
+                    nthreads=nthreads, want_pre=want_pre)
+
+
+def gemm_ex_entries(A, B, rows, cols, dtype="f16", alpha=1.0, beta=0.0, C=None, bias=None, relu=False,
+                    nthreads=None, oracle=None):
+    """D at the listed (row, col) entries."""
+    return _gemm_ex(oracle or default(), A, B, dtype, alpha, beta, C, bias, relu, rows=rows, cols=cols,
+                    nthreads=nthreads)
+
+
+def bf16_to_f64(bits):
+    return default().bf16_to_f64(bits)
+
+
+def f64_to_bf16(x):
+    return default().f64_to_bf16(x)

@@ -102,6 +102,60 @@ static uint16_t f16_encode(double x) {
     return sign | (uint16_t)(expo << 10) | (uint16_t)(n - 1024);
 }
 
+/* ------------------------------------------------------------------ */
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits --  */
+/* the top half of an IEEE binary32 (the GEMM blog post, section 2.2,     */
+/* lists it beside fp16: same size, binary32's exponent range).           */
+/*   exponent field 0      : subnormal, value = frac * 2^-133             */
+/*   exponent field 1..254 : normal,    value = (128 + frac) * 2^(e - 134)*/
+/*   exponent field 255    : infinity (frac == 0) or NaN.                 */
+/* In the binade [2^E, 2^(E+1)), E >= -126, values are 2^(E-7) apart;     */
+/* below 2^-126 they are 2^-133 apart.  Largest finite: 255 * 2^120.      */
+/* ------------------------------------------------------------------ */
+static double bf16_decode(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 7) & 0xFF;
+    const int frac = h & 0x7F;
+    double v;
+    if (expo == 0) v = ldexp((double)frac, -133);
+    else if (expo == 255) v = frac ? NAN : INFINITY;
+    else v = ldexp((double)(128 + frac), expo - 134);
+    return sign ? -v : v;
+}
+
+static uint16_t bf16_encode(double x) {
+    uint64_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    const uint16_t sign = (uint16_t)((bits >> 48) & 0x8000u);
+    const int eb = (int)((bits >> 52) & 0x7FF);
+    const uint64_t man = bits & 0x000FFFFFFFFFFFFFull;
+    if (eb == 0x7FF) {
+        if (man == 0) return sign | 0x7F80u;
+        return sign | 0x7FC0u;                            /* a quiet NaN */
+    }
+    if (eb == 0) return sign;                             /* below 2^-1022: rounds to zero */
+    const uint64_t sig = (1ull << 52) | man;              /* |x| = sig * 2^(eb - 1075) */
+    const int E = eb - 1023;
+    if (E >= 128) return sign | 0x7F80u;                  /* >= 2^128: overflow */
+    const int q = (E > -126 ? E : -126) - 7;              /* spacing 2^q around |x| */
+    const int s = q + 1075 - eb;                          /* >= 45 */
+    uint64_t n;
+    if (s >= 64) {
+        n = 0;
+    } else {
+        n = sig >> s;
+        const uint64_t rem = sig & ((1ull << s) - 1);
+        const uint64_t half = 1ull << (s - 1);
+        if (rem > half || (rem == half && (n & 1))) n += 1;  /* nearest, ties to even */
+    }
+    int qq = q;
+    if (qq == -133 && n < 128) return sign | (uint16_t)n;    /* subnormal or zero */
+    if (n == 256) { n = 128; qq += 1; }
+    const int expo = qq + 7 + 127;
+    if (expo >= 255) return sign | 0x7F80u;
+    return sign | (uint16_t)(expo << 7) | (uint16_t)(n - 128);
+}
+
 /* Decode table built from f16_decode, so the inner loop does not re-derive
  * each value.  Built once, thread-safely. */
 static double g_decode[65536];
@@ -112,6 +166,16 @@ static void build_decode_table(void) {
 static const double* decode_table(void) {
     pthread_once(&g_decode_once, build_decode_table);
     return g_decode;
+}
+
+static double g_decode_bf16[65536];
+static pthread_once_t g_decode_bf16_once = PTHREAD_ONCE_INIT;
+static void build_decode_bf16_table(void) {
+    for (uint32_t h = 0; h < 65536u; ++h) g_decode_bf16[h] = bf16_decode((uint16_t)h);
+}
+static const double* decode_bf16_table(void) {
+    pthread_once(&g_decode_bf16_once, build_decode_bf16_table);
+    return g_decode_bf16;
 }
 
 /* One element of the definition: ascending k, one fp64 accumulator. */
@@ -130,6 +194,14 @@ void oracle_f16_to_f64(const uint16_t* h, double* out, int64_t n) {
 
 void oracle_f64_to_f16(const double* x, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = f16_encode(x[i]);
+}
+
+void oracle_bf16_to_f64(const uint16_t* h, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bf16_decode(h[i]);
+}
+
+void oracle_f64_to_bf16(const double* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bf16_encode(x[i]);
 }
 
 /* ------------------------------------------------------------------ */
@@ -232,4 +304,106 @@ int oracle_gemm_nt_rows(const uint16_t* A, const uint16_t* B, int64_t M, int64_t
     j.row_begin = row_begin; j.row_end = row_end;
     j.sums = sums; j.out = out; j.nthreads = nthreads;
     return run_threads(&j, rows_worker);
+}
+
+/* ------------------------------------------------------------------ */
+/* exported: GEMM with an element type and the fused output transform  */
+/*   D[m,n] = round( act( alpha * S[m,n] + beta * C[m,n] + bias[n] ) )  */
+/* with S the plain definition above (fp64, ascending k), every term in */
+/* fp64 and one rounding to the element type at the end.  This is the  */
+/* scaled update C = alpha A B + beta C of the GEMM blog post (section  */
+/* 2.1) with the bias and ReLU fusion it recommends (section 5.4).      */
+/* dtype 0 = fp16, 1 = bf16; C and bias may be NULL; act 0 none, 1 relu. */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int dtype;
+    const uint16_t* A;
+    const uint16_t* B;
+    int64_t M, N, K;
+    const int64_t* rows;
+    const int64_t* cols;
+    int64_t count;
+    int64_t row_begin, row_end;
+    double alpha, beta;
+    const uint16_t* C;
+    const uint16_t* bias;
+    int act;
+    double* pre;          /* optional: the value before rounding */
+    uint16_t* out;
+    int nthreads;
+    int tid;
+    int rows_mode;
+} job_ex_t;
+
+static double element_ex(const job_ex_t* j, const double* dec, int64_t m, int64_t n) {
+    double v = j->alpha * dot_row_row(dec, j->A + m * j->K, j->B + n * j->K, j->K);
+    if (j->C && j->beta != 0.0) v += j->beta * dec[j->C[m * j->N + n]];
+    if (j->bias) v += dec[j->bias[n]];
+    if (j->act == 1 && v < 0.0) v = 0.0;   /* relu: negative values to zero; NaN and -0 pass */
+    return v;
+}
+
+static void* ex_worker(void* p) {
+    job_ex_t* j = (job_ex_t*)p;
+    const double* dec = j->dtype == 1 ? decode_bf16_table() : decode_table();
+    const int64_t total = j->rows_mode ? (j->row_end - j->row_begin) * j->N : j->count;
+    const int64_t lo = total * j->tid / j->nthreads;
+    const int64_t hi = total * (j->tid + 1) / j->nthreads;
+    for (int64_t i = lo; i < hi; ++i) {
+        int64_t m, n;
+        if (j->rows_mode) { m = j->row_begin + i / j->N; n = i % j->N; }
+        else { m = j->rows[i]; n = j->cols[i]; }
+        const double v = element_ex(j, dec, m, n);
+        if (j->pre) j->pre[i] = v;
+        j->out[i] = j->dtype == 1 ? bf16_encode(v) : f16_encode(v);
+    }
+    return NULL;
+}
+
+static int run_ex(job_ex_t* proto) {
+    int nt = proto->nthreads < 1 ? 1 : proto->nthreads;
+    if (nt > 1024) nt = 1024;
+    proto->nthreads = nt;
+    job_ex_t* jobs = (job_ex_t*)malloc(sizeof(job_ex_t) * (size_t)nt);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!jobs || !th) { free(jobs); free(th); return -1; }
+    int started = 0;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t] = *proto;
+        jobs[t].tid = t;
+        if (t == 0) continue;
+        if (pthread_create(&th[t], NULL, ex_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    ex_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = started + 1; t < nt; ++t) ex_worker(&jobs[t]);
+    free(jobs);
+    free(th);
+    return 0;
+}
+
+/* Entries (rows[i], cols[i]) when rows != NULL, else rows [row_begin,
+ * row_end) written row-major.  Returns 0, or -1 on bad arguments. */
+int oracle_gemm_nt_ex(int dtype, const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                      const int64_t* rows, const int64_t* cols, int64_t count,
+                      int64_t row_begin, int64_t row_end,
+                      double alpha, double beta, const uint16_t* C, const uint16_t* bias, int act,
+                      double* pre, uint16_t* out, int nthreads) {
+    if ((dtype != 0 && dtype != 1) || M < 0 || N < 0 || K < 0 || (act != 0 && act != 1)) return -1;
+    job_ex_t j;
+    memset(&j, 0, sizeof j);
+    if (rows) {
+        if (count < 0) return -1;
+        for (int64_t i = 0; i < count; ++i)
+            if (rows[i] < 0 || rows[i] >= M || cols[i] < 0 || cols[i] >= N) return -1;
+        j.rows = rows; j.cols = cols; j.count = count;
+    } else {
+        if (row_begin < 0 || row_end > M || row_begin > row_end) return -1;
+        j.rows_mode = 1; j.row_begin = row_begin; j.row_end = row_end;
+    }
+    j.dtype = dtype; j.A = A; j.B = B; j.M = M; j.N = N; j.K = K;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.bias = bias; j.act = act;
+    j.pre = pre; j.out = out; j.nthreads = nthreads;
+    return run_ex(&j);
 }

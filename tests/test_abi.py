@@ -87,6 +87,34 @@ def test_argument_errors_are_returned_before_any_device_call(lib):
     assert st in (S.ERR_CUDA, S.ERR_UNSUPPORTED_DEVICE, S.OK)
 
 
+def _call_ex(M, N, K, dtype=0, alpha=1.0, beta=0.0, C=None, bias=None, act=0, variant=0,
+             A=FAKE, B=FAKE + (1 << 32), D=FAKE + (2 << 32), epilogue=True):
+    lib = g.load()
+    epi = g.Epilogue(alpha, beta, C, bias, act, 0)
+    return lib.gemm_nt_ex(dtype, A, B, D, M, N, K, ctypes.byref(epi) if epilogue else None, variant, None)
+
+
+def test_epilogue_argument_errors_are_returned_before_any_device_call(lib):
+    S = g.Status
+    D = FAKE + (2 << 32)
+    assert _call_ex(8, 8, 8, dtype=2) == S.ERR_INVALID_VALUE            # unknown element type
+    assert _call_ex(8, 8, 8, dtype=-1, epilogue=False) == S.ERR_INVALID_VALUE
+    assert _call_ex(8, 8, 8, act=2) == S.ERR_INVALID_VALUE              # unknown activation
+    assert _call_ex(8, 8, 8, beta=1.0) == S.ERR_INVALID_VALUE           # beta != 0 needs C
+    assert _call_ex(8, 8, 8, beta=1.0, C=FAKE + (3 << 32) + 2) == S.ERR_MISALIGNED
+    assert _call_ex(8, 8, 8, bias=FAKE + (3 << 32) + 8) == S.ERR_MISALIGNED
+    assert _call_ex(8, 8, 8, beta=1.0, C=D + 16) == S.ERR_INVALID_VALUE  # C partly over D
+    assert _call_ex(8, 8, 8, bias=D + 32) == S.ERR_INVALID_VALUE         # bias inside D
+    # beta == 0: C is never read, so a misaligned or overlapping C is no error
+    assert _call_ex(0, 8, 8, beta=0.0, C=FAKE + 2) == S.OK
+    # empty problems stay a no-op with an epilogue
+    assert _call_ex(0, 8, 8, beta=1.0, C=FAKE, A=0, B=0, D=0) == S.OK
+    assert _call_ex(8, 0, 8, dtype=1, bias=FAKE, A=0, B=0, D=0) == S.OK
+    # the plain bf16 entry point shares the operand checks
+    assert lib.gemm_bf16_nt(FAKE + 2, FAKE + (1 << 32), D, 8, 8, 8, None) == S.ERR_MISALIGNED
+    assert lib.gemm_bf16_nt(FAKE, FAKE + (1 << 32), D, 8, 8, 12, None) == S.ERR_MISALIGNED
+
+
 def test_python_binding_rejects_bad_arguments(lib):
     with pytest.raises(ValueError):
         g.gemm_f16_nt(FAKE, FAKE, FAKE)          # raw pointers without sizes
