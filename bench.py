@@ -54,6 +54,10 @@ def parse_args():
                     help="time an M x N x K problem (normal(0, 1/sqrt(K)) entries) instead of a named workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                    help="operand and output type (bf16 runs the same kernels with bf16 operands)")
+    ap.add_argument("--epilogue", action="store_true",
+                    help="time D = relu(1.5 * A·Bᵀ + 0.5 * C + bias) through gemm_nt_ex instead of the plain product")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -162,29 +166,40 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None):
-    """Time the oracle on a block of output rows sized to take about target_s."""
+def oracle_rows_fn(A, B, dtype="f16", epi=None):
+    """f(r0, r1, threads): the oracle's rows r0..r1-1 of D for this bench configuration."""
     import oracle
     o = oracle.default()
+    if dtype == "f16" and epi is None:
+        return lambda r0, r1, threads: o.gemm_rows(A, B, r0, r1, nthreads=threads)
+    C, bias = epi if epi is not None else (None, None)
+    alpha, beta, relu = (EPI_ALPHA, EPI_BETA, True) if epi is not None else (1.0, 0.0, False)
+    return lambda r0, r1, threads: oracle._gemm_ex(o, A, B, dtype, alpha, beta, C, bias, relu,
+                                                   row_begin=r0, row_end=r1, nthreads=threads)
+
+
+def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None, dtype="f16", epi=None):
+    """Time the oracle on a block of output rows sized to take about target_s."""
+    import oracle
     threads = oracle.default_threads()
+    fn = oracle_rows_fn(A, B, dtype, epi)
     M, K = A.shape
-    N = B.shape[0]
     t = time.perf_counter()
-    o.gemm_rows(A, B, 0, 1, nthreads=threads)
+    fn(0, 1, threads)
     one = max(time.perf_counter() - t, 1e-4)
     rows = int(max(1, min(M, target_s / one)))
     if max_rows:
         rows = min(rows, max_rows)
     t = time.perf_counter()
-    o.gemm_rows(A, B, 0, rows, nthreads=threads)
+    fn(0, rows, threads)
     dt = time.perf_counter() - t
     return rows, dt, threads
 
 
-def cpu_baseline(A, B, target_s: float) -> dict:
+def cpu_baseline(A, B, target_s: float, dtype="f16", epi=None) -> dict:
     M, K = A.shape
     N = B.shape[0]
-    rows, dt, threads = oracle_rows_timing(A, B, target_s)
+    rows, dt, threads = oracle_rows_timing(A, B, target_s, dtype=dtype, epi=epi)
     return {"value": metrics.tflops(rows, N, K, dt), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of D ({rows}x{N} outputs, K={K}) of the same seeded "
                       f"operands, fp64 accumulation, {dt:.2f} s"}
@@ -197,8 +212,19 @@ def workload_of(args):
     return inputs.WORKLOADS[args.workload]
 
 
-def operands_of(w):
+def operands_of(w, dtype="f16"):
+    if dtype == "bf16":
+        return inputs.operands_bf16(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
     return inputs.operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
+
+
+EPI_ALPHA, EPI_BETA = 1.5, 0.5
+
+
+def epilogue_inputs(w, dtype="f16"):
+    """C [M, N] and bias [N] of the fused-epilogue timing, uniform(-1, 1), seeded."""
+    drawf = inputs.draw_bf16 if dtype == "bf16" else inputs.draw
+    return drawf(w.M, w.N, "uniform", w.seed + 2000), drawf(1, w.N, "uniform", w.seed + 3000).reshape(w.N)
 
 
 def run_reference(args):
@@ -206,25 +232,25 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = workload_of(args)
-    A, B = operands_of(w)
+    A, B = operands_of(w, args.dtype)
     import oracle
-    o = oracle.default()
     threads = oracle.default_threads()
+    fn = oracle_rows_fn(A, B, args.dtype, epilogue_inputs(w, args.dtype) if args.epilogue else None)
     # bound the whole run to a few minutes: size each step's sample of rows
     budget = 120.0
     per_step = max(0.05, min(2.0, budget / max(1, args.steps + args.warmup)))
     t = time.perf_counter()
-    o.gemm_rows(A, B, 0, 1, nthreads=threads)
+    fn(0, 1, threads)
     one = max(time.perf_counter() - t, 1e-4)
     rows = int(max(1, min(w.M, per_step / one)))
     for i in range(args.warmup):
         r0 = (i * rows) % max(1, w.M - rows + 1)
-        o.gemm_rows(A, B, r0, r0 + rows, nthreads=threads)
+        fn(r0, r0 + rows, threads)
     times = []
     for i in range(args.steps):
         r0 = (i * rows) % max(1, w.M - rows + 1)
         t = time.perf_counter()
-        o.gemm_rows(A, B, r0, r0 + rows, nthreads=threads)
+        fn(r0, r0 + rows, threads)
         times.append(time.perf_counter() - t)
     sec = sum(times) / len(times)
     value = metrics.tflops(rows, w.N, w.K, sec)
@@ -232,7 +258,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "operands": args.dtype,
+                   "epilogue": (f"relu({EPI_ALPHA} * A·Bᵀ + {EPI_BETA} * C + bias)" if args.epilogue else "none"),
                    "sample_rows_per_step": rows, "note": "CPU oracle on a bounded sample of rows"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{rows} rows of D per step ({rows}x{w.N} outputs, K={w.K})"},
@@ -262,20 +289,45 @@ def run_ours(args):
     gbuild.build()
     g.load()
     w = workload_of(args)
-    A_h, B_h = operands_of(w)
+    A_h, B_h = operands_of(w, args.dtype)
+    tdt = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+
+    def to_torch(x):
+        # bf16 operands travel as uint16 bit patterns
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if args.dtype == "bf16" else x)
+        return t.view(tdt)
+
     stream = torch.cuda.Stream(device=dev)
-    A = torch.from_numpy(A_h).to(dev)
-    B = torch.from_numpy(B_h).to(dev)
-    D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    A = to_torch(A_h).to(dev)
+    B = to_torch(B_h).to(dev)
+    D = torch.empty((w.M, w.N), dtype=tdt, device=dev)
     plan = g.gemm_f16_nt_plan(w.M, w.N, w.K)
     lib = g.load()
     s_handle = stream.cuda_stream
     a_ptr, b_ptr, d_ptr = A.data_ptr(), B.data_ptr(), D.data_ptr()
+    C_h = bias_h = C = bias = None
+    if args.epilogue:
+        C_h, bias_h = epilogue_inputs(w, args.dtype)
+        C, bias = to_torch(C_h).to(dev), to_torch(bias_h).to(dev)
+        epi = g.Epilogue(EPI_ALPHA, EPI_BETA, C.data_ptr(), bias.data_ptr(), int(g.Activation.RELU), 0)
+        epi_ref = g.ctypes.byref(epi)
+    dtype_code = int(g.Dtype.BF16 if args.dtype == "bf16" else g.Dtype.F16)
 
-    def step():
-        st = lib.gemm_f16_nt(a_ptr, b_ptr, d_ptr, w.M, w.N, w.K, s_handle)
-        if st != 0:
-            raise g.GemmError(st, "gemm_f16_nt")
+    if args.epilogue:
+        def step():
+            st = lib.gemm_nt_ex(dtype_code, a_ptr, b_ptr, d_ptr, w.M, w.N, w.K, epi_ref, 0, s_handle)
+            if st != 0:
+                raise g.GemmError(st, "gemm_nt_ex")
+    elif args.dtype == "bf16":
+        def step():
+            st = lib.gemm_bf16_nt(a_ptr, b_ptr, d_ptr, w.M, w.N, w.K, s_handle)
+            if st != 0:
+                raise g.GemmError(st, "gemm_bf16_nt")
+    else:
+        def step():
+            st = lib.gemm_f16_nt(a_ptr, b_ptr, d_ptr, w.M, w.N, w.K, s_handle)
+            if st != 0:
+                raise g.GemmError(st, "gemm_f16_nt")
 
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -316,15 +368,18 @@ def run_ours(args):
     # end to end through the C ABI: pinned host operands in, pinned host result out
     e2e = None
     if not args.no_e2e:
-        A_pin = torch.from_numpy(A_h).pin_memory()
-        B_pin = torch.from_numpy(B_h).pin_memory()
-        D_pin = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+        A_pin = to_torch(A_h).pin_memory()
+        B_pin = to_torch(B_h).pin_memory()
+        D_pin = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
+        host_in = [(A, A_pin), (B, B_pin)]
+        if args.epilogue:
+            host_in += [(C, to_torch(C_h).pin_memory()), (bias, to_torch(bias_h).pin_memory())]
         e2e_steps = max(3, min(args.steps, 20))
 
         def e2e_step():
             with torch.cuda.stream(stream):
-                A.copy_(A_pin, non_blocking=True)
-                B.copy_(B_pin, non_blocking=True)
+                for dst, src in host_in:
+                    dst.copy_(src, non_blocking=True)
                 step()
                 D_pin.copy_(D, non_blocking=True)
 
@@ -346,7 +401,7 @@ def run_ours(args):
         g.gemm_f16_nt_check(stream=stream, device=dev)
         e2e = {"value": world * metrics.tflops(w.M, w.N, w.K, e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": A_pin.numel() * 2 + B_pin.numel() * 2,
+               "h2d_bytes_per_step": sum(src.numel() * 2 for _, src in host_in),
                "d2h_bytes_per_step": D_pin.numel() * 2}
 
     clocks = sampler.stop() if sampler else None
@@ -365,24 +420,29 @@ def run_ours(args):
         peak = FALLBACK_PEAK_TFLOPS
         peak_src = "fallback"
     achieved = metrics.tflops(w.M, w.N, w.K, launch_ms * 1e-3)
+    # the ncu counters were taken on the plain fp16 product
+    traffic = recorded_traffic(w.name) if args.dtype == "f16" and not args.epilogue else None
     if plan["variant"] == "SKINNY_SPLITK":
         hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else 6800.0
-        gbs = metrics.gbs(w.compulsory_bytes, launch_ms * 1e-3)
+        # algorithmic bytes: A and B read once, D written once (+ C and bias read with the epilogue)
+        alg_bytes = w.compulsory_bytes + (w.M * w.N * 2 + w.N * 2 if args.epilogue else 0)
+        gbs = metrics.gbs(alg_bytes, launch_ms * 1e-3)
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                    "traffic": recorded_traffic(w.name), "peak_source": "measured" if peaks else "fallback"}
+                    "traffic": traffic, "peak_source": "measured" if peaks else "fallback"}
     else:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": recorded_traffic(w.name), "peak_source": peak_src}
+                    "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(A_h, B_h, args.cpu_seconds)
+        cpu = cpu_baseline(A_h, B_h, args.cpu_seconds, args.dtype, (C_h, bias_h) if args.epilogue else None)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "accumulate": "f32",
+                   "epilogue": (f"relu({EPI_ALPHA} * A·Bᵀ + {EPI_BETA} * C + bias)" if args.epilogue else "none"),
                    "variant": plan["variant"], "grid_ctas": plan["grid_ctas"],
                    "l2": "inputs larger than L2 (A+B = %d MiB > 129 MB); no flush" %
                          ((w.M * w.K + w.N * w.K) * 2 >> 20) if (w.M * w.K + w.N * w.K) * 2 > 129e6

@@ -62,16 +62,23 @@ struct Elem<__nv_bfloat16> {
     __device__ __forceinline__ static float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
-// Applies the fused transform to 8 consecutive columns [col, col + 8) of one
-// output row; col is a multiple of 8 (N % 8 == 0 keeps the 16-byte loads in
-// bounds and aligned).  Rows at or past M read no C.
+// The 8 C values at [row][col, col + 8) as one 16-byte load (zero when C is
+// not read or the row is past M).  col is a multiple of 8 (N % 8 == 0 keeps
+// the load in bounds and aligned).  Issued ahead of its use, its latency
+// hides behind the TMEM reads.
 template <class T>
-__device__ __forceinline__ void epi_apply8(const EpiParams& e, float (&x)[8], int64_t row, int64_t col,
-                                           int64_t M, int64_t N) {
+__device__ __forceinline__ uint4 epi_load_c8(const EpiParams& e, int64_t row, int64_t col, int64_t M, int64_t N) {
+    if (e.C == nullptr || e.beta == 0.0f || row >= M) return make_uint4(0u, 0u, 0u, 0u);
+    return *reinterpret_cast<const uint4*>(static_cast<const T*>(e.C) + row * N + col);
+}
+
+// Applies the fused transform to 8 consecutive columns [col, col + 8) of one
+// output row, given that row's C values from epi_load_c8.
+template <class T>
+__device__ __forceinline__ void epi_apply8_c(const EpiParams& e, float (&x)[8], uint4 c, int64_t col) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] *= e.alpha;
-    if (e.C != nullptr && e.beta != 0.0f && row < M) {
-        const uint4 c = *reinterpret_cast<const uint4*>(static_cast<const T*>(e.C) + row * N + col);
+    if (e.C != nullptr && e.beta != 0.0f) {
         const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -104,5 +111,34 @@ __device__ __forceinline__ float epi_apply1(const EpiParams& e, float x, int64_t
     if (e.act == 1) x = x < 0.0f ? 0.0f : x;
     return x;
 }
+
+// One output column n of the small-M kernel (rows 0..MN-1): the C values and
+// the bias are fetched with independent loads before any output is written,
+// so their latencies overlap (and an in-place C == D is read before it is
+// overwritten).  apply() is epi_apply1 on the fetched values.
+// The C values stay in their 16-bit form, two to a register.
+template <class T, int MN>
+struct EpiColumn {
+    uint32_t c[(MN + 1) / 2];
+    float b;
+    __device__ __forceinline__ void load(const EpiParams& e, int64_t n, int64_t M, int64_t N) {
+        const bool use_c = e.C != nullptr && e.beta != 0.0f;
+        const uint16_t* C = static_cast<const uint16_t*>(e.C);
+#pragma unroll
+        for (int i = 0; i < (MN + 1) / 2; ++i) c[i] = 0u;
+#pragma unroll
+        for (int m = 0; m < MN; ++m)
+            if (use_c && m < M) c[m >> 1] |= static_cast<uint32_t>(C[m * N + n]) << (16 * (m & 1));
+        b = e.bias != nullptr ? Elem<T>::to_float(static_cast<const T*>(e.bias)[n]) : 0.0f;
+    }
+    __device__ __forceinline__ float apply(const EpiParams& e, float x, int m) const {
+        x *= e.alpha;
+        if (e.C != nullptr && e.beta != 0.0f)
+            x += e.beta * ((m & 1) ? Elem<T>::hi(c[m >> 1]) : Elem<T>::lo(c[m >> 1]));
+        if (e.bias != nullptr) x += b;
+        if (e.act == 1) x = x < 0.0f ? 0.0f : x;
+        return x;
+    }
+};
 
 }  // namespace gemm_gb300

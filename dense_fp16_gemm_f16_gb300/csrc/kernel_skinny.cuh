@@ -192,13 +192,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (c_first == c_last) {
                 // the whole K loop of this tile ran here
                 if (n < p.N) {
+                    if (p.epi.on) {
+                        EpiColumn<T, MN> ec;
+                        ec.load(p.epi, n, p.M, p.N);
 #pragma unroll
-                    for (int m = 0; m < MN; ++m) {
-                        if (m < p.M) {
-                            float x = __uint_as_float(v[m]);
-                            if (p.epi.on) x = epi_apply1<T>(p.epi, x, m, n, p.N);
-                            D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
-                        }
+                        for (int m = 0; m < MN; ++m)
+                            if (m < p.M)
+                                D[m * static_cast<int64_t>(p.N) + n] =
+                                    Elem<T>::from_float(ec.apply(p.epi, __uint_as_float(v[m]), m));
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < MN; ++m)
+                            if (m < p.M) D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(__uint_as_float(v[m]));
                     }
                 }
             } else {
@@ -232,6 +237,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const bool self_in_regs = (*last_flag == 2u);
                     __threadfence();
                     if (n < p.N) {
+                        EpiColumn<T, MN> ec;
+                        if (p.epi.on) ec.load(p.epi, n, p.M, p.N);   // in flight during the sum
                         // Sum the pieces in ascending CTA order.  Pieces are fetched
                         // CH at a time with independent loads so their latencies
                         // overlap; the additions keep the fixed order.
@@ -264,7 +271,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
                         for (int m = 0; m < MN; ++m) {
                             if (m < p.M) {
-                                const float x = p.epi.on ? epi_apply1<T>(p.epi, acc[m], m, n, p.N) : acc[m];
+                                const float x = p.epi.on ? ec.apply(p.epi, acc[m], m) : acc[m];
                                 D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
                             }
                         }

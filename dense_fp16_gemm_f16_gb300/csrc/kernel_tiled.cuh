@@ -56,10 +56,15 @@ __device__ __forceinline__ void split_k_reduce_row(const float* base, int r_loca
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 8 * GB) {
         float acc[GB][8];
+        uint4 cv[GB];   // C values, in flight with the partials
 #pragma unroll
-        for (int g = 0; g < GB; ++g)
+        for (int g = 0; g < GB; ++g) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[g][e] = 0.0f;
+            const int64_t gcol = n0 + c + 8 * g;
+            cv[g] = (p.epi.on && c + 8 * g < c_end && gcol < p.N) ? epi_load_c8<T>(p.epi, grow, gcol, p.M, p.N)
+                                                                 : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int j0 = 0; j0 < S; j0 += JC) {
             float4 pv[GB][JC][2];
@@ -93,7 +98,7 @@ __device__ __forceinline__ void split_k_reduce_row(const float* base, int r_loca
             const int cg = c + 8 * g;
             const int64_t gcol = n0 + cg;
             if (cg < c_end && gcol < p.N) {         // N % 8 == 0: groups are all in or all out
-                if (p.epi.on) epi_apply8<T>(p.epi, acc[g], grow, gcol, p.M, p.N);
+                if (p.epi.on) epi_apply8_c<T>(p.epi, acc[g], cv[g], gcol);
                 uint32_t h[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(acc[g][2 * e], acc[g][2 * e + 1]);
@@ -377,6 +382,16 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
+                const int64_t col0 = n0 + c * Cfg::EPI_COLS;
+                const bool store = rows_in && col0 < p.N;  // warp-uniform
+                // this chunk's C values, in flight while TMEM is read
+                uint4 cv[8];
+                if (p.epi.on) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        cv[j] = (store && col0 + 8 * j < p.N) ? epi_load_c8<T>(p.epi, row0 + lane, col0 + 8 * j, p.M, p.N)
+                                                             : make_uint4(0u, 0u, 0u, 0u);
+                }
                 uint32_t v[64];
                 ptx::tmem_ld_x32(t_row + c * 64, v);
                 ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
@@ -390,8 +405,6 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         else ptx::mbar_arrive(tempty_bar(buf));
                     }
                 }
-                const int64_t col0 = n0 + c * Cfg::EPI_COLS;
-                const bool store = rows_in && col0 < p.N;  // warp-uniform
                 // the TMA store issued two chunks ago from this buffer has read it
                 if (lane == 0) ptx::bulk_wait_group_read<1>();
                 __syncwarp();
@@ -405,8 +418,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         float x[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * j + e]);
-                        if (p.epi.on && col0 + 8 * j < p.N)
-                            epi_apply8<T>(p.epi, x, row0 + lane, col0 + 8 * j, p.M, p.N);
+                        if (p.epi.on && col0 + 8 * j < p.N) epi_apply8_c<T>(p.epi, x, cv[j], col0 + 8 * j);
                         uint32_t h[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(x[2 * e], x[2 * e + 1]);
