@@ -463,7 +463,10 @@ def run_ours(args):
                    "l2": (f"inputs larger than L2 (A+B = {ab_bytes >> 20} MiB >= {L2_ROTATE_BYTES >> 20} MiB); no flush"
                           if copies == 1 else
                           f"A and B rotated over {copies} copies ({copies * ab_bytes >> 20} MiB, > 2x the 129 MB L2) "
-                          "so no launch finds its operands in L2; no flush"),
+                          "so no launch finds its operands in L2; no flush"
+                          if copies * ab_bytes >= L2_ROTATE_BYTES else
+                          f"A and B rotated over {copies} copies ({copies * ab_bytes / 2**20:.1f} MiB), still within "
+                          "L2: a warm-L2 number"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "timing": "one CUDA event pair around the K back-to-back launches on the launch stream"},
         "roofline": roofline,

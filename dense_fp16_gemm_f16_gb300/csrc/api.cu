@@ -452,6 +452,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         p.epi = epi;
         p.status = dev->status;
         p.timeout_ns = timeout_for(pl.k_blocks);
+        p.stream_b = N * K * 2 >= kStreamBBytes ? 1 : 0;
         if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
@@ -593,6 +594,7 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
     p.epi = epi_params(nullptr);
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
+    p.stream_b = N * K * 2 >= kStreamBBytes ? 1 : 0;
     if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

@@ -29,6 +29,18 @@ constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
 
 GEMM_HD int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// a / b for a >= 0, b > 0.  On the device a 64-bit division is a long
+// software sequence; when both fit in 32 bits (every realistic problem) the
+// 32-bit division gives the same quotient much faster.
+GEMM_HD int64_t div_nonneg(int64_t a, int64_t b) {
+#if defined(__CUDA_ARCH__)
+    if ((static_cast<uint64_t>(a) | static_cast<uint64_t>(b)) <= 0xFFFFFFFFull)
+        return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+#endif
+    return a / b;
+}
+
+
 // ------------------------------------------------------------------ tiled
 // Persistent, warp-specialised kernel.  CG = CTAs per MMA (1, or 2 for a
 // cta_group::2 pair in a 2-CTA cluster), BN = output columns per tile.  A tile
@@ -97,12 +109,12 @@ struct TiledParams {
 GEMM_HD void tile_coords(int64_t t, int64_t m_tiles, int64_t n_tiles, int64_t group_m,
                          int64_t& tm, int64_t& tn) {
     const int64_t per_group = group_m * n_tiles;
-    const int64_t g = t / per_group;
+    const int64_t g = div_nonneg(t, per_group);
     const int64_t first_m = g * group_m;
     const int64_t rows = (m_tiles - first_m < group_m) ? (m_tiles - first_m) : group_m;
     const int64_t r = t - g * per_group;
-    tm = first_m + r % rows;
-    tn = r / rows;
+    tn = div_nonneg(r, rows);
+    tm = first_m + (r - tn * rows);
 }
 
 // Bytes per ring stage of a launch: a whole [A | B] stage, or, when every
@@ -121,14 +133,14 @@ GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int
     kb1 = p.k_blocks;
     if (p.ksplit > 1) {
         // split-K: unit u is piece j of tile t; the pieces split the K blocks evenly
-        const int64_t t = u / p.ksplit;
+        const int64_t t = div_nonneg(u, p.ksplit);
         const int j = static_cast<int>(u - t * p.ksplit);
         int64_t tn;
         tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
         nw = BN;
         n0 = tn * BN;
-        kb0 = static_cast<int>(static_cast<int64_t>(j) * p.k_blocks / p.ksplit);
-        kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.k_blocks / p.ksplit);
+        kb0 = static_cast<int>(div_nonneg(static_cast<int64_t>(j) * p.k_blocks, p.ksplit));
+        kb1 = static_cast<int>(div_nonneg(static_cast<int64_t>(j + 1) * p.k_blocks, p.ksplit));
         return;
     }
     int64_t t = u, piece = 0;
@@ -136,8 +148,9 @@ GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int
     if (u >= p.num_full) {
         const int64_t v = u - p.num_full;
         s = p.split;
-        t = p.num_full + v / s;
-        piece = v - (v / s) * s;
+        const int64_t q = div_nonneg(v, s);
+        t = p.num_full + q;
+        piece = v - q * s;
     }
     int64_t tn;
     tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
@@ -224,14 +237,20 @@ struct SkinnyParams {
     EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
     uint32_t* status;
     uint64_t timeout_ns;
+    int32_t stream_b;         // B is too large to stay in L2: load it evict-first
 };
 
+// B of at least this many bytes is read once per call and cannot stay in the
+// 129 MB L2 until the next one, so the small-M kernel streams it with an
+// evict-first policy (keeping A and the fp32 partials in L2 instead).
+constexpr int64_t kStreamBBytes = 96ll << 20;
+
 // First unit of CTA c's range; CTA c owns [unit_begin(c), unit_begin(c+1)).
-GEMM_HD int64_t unit_begin(int64_t c, int64_t units, int64_t G) { return c * units / G; }
+GEMM_HD int64_t unit_begin(int64_t c, int64_t units, int64_t G) { return div_nonneg(c * units, G); }
 
 // The CTA whose range holds unit u.
 GEMM_HD int64_t cta_of_unit(int64_t u, int64_t units, int64_t G) {
-    return ((u + 1) * G - 1) / units;
+    return div_nonneg((u + 1) * G - 1, units);
 }
 
 }  // namespace gemm_gb300

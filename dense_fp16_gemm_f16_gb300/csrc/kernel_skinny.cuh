@@ -104,17 +104,21 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
+            // B streams past (evict first when it cannot stay in L2); A is
+            // re-read by every CTA and stays
+            const uint64_t pol_w = p.stream_b ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+            const uint64_t pol_x = ptx::policy_evict_last();
             for (int64_t u = u0; u < u1; ++u) {
-                const int64_t t = u / KB;
+                const int64_t t = div_nonneg(u, KB);
                 const int32_t kx = static_cast<int32_t>((u - t * KB) * kBK);
                 if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
-                ptx::tma_load_2d(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES, &tmW, full_bar(stage), kx,
-                                 static_cast<int32_t>(t * 128));
-                ptx::tma_load_2d(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES, &tmX, full_bar(stage), kx, 0);
+                ptx::tma_load_2d_hint(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES, &tmW, full_bar(stage), kx,
+                                      static_cast<int32_t>(t * 128), pol_w);
+                ptx::tma_load_2d_hint(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES, &tmX, full_bar(stage), kx, 0, pol_x);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             for (int i = 0; ok && i < STAGES; ++i) {
@@ -130,7 +134,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint32_t phase = 0;
             uint32_t seg = 0;
             for (int64_t u = u0; ok && u < u1; ++seg) {
-                const int64_t t = u / KB;
+                const int64_t t = div_nonneg(u, KB);
                 const int64_t seg_end = (t + 1) * KB < u1 ? (t + 1) * KB : u1;
                 const uint32_t buf = seg & 1u;
                 const uint32_t use = (seg >> 1) & 1u;
@@ -167,10 +171,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int r = q * 32 + lane;                     // row of the 128-row tile = output column
         const int etid = threadIdx.x - 64;               // 0..127 among the epilogue threads
         T* D = static_cast<T*>(p.D);
-        const int64_t first_tile = u0 / KB;
+        const int64_t first_tile = div_nonneg(u0, KB);
         uint32_t seg = 0;
         for (int64_t u = u0; u < u1; ++seg) {
-            const int64_t t = u / KB;
+            const int64_t t = div_nonneg(u, KB);
             const int64_t seg_end = (t + 1) * KB < u1 ? (t + 1) * KB : u1;
             const uint32_t buf = seg & 1u;
             const uint32_t use = (seg >> 1) & 1u;
@@ -222,9 +226,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 if (!(owner && *last_flag == 2u)) {
                     float* mine = p.partials +
                                   ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
+                    const uint64_t pol_keep = ptx::policy_evict_last();   // read back soon by the reducer
 #pragma unroll
                     for (int m = 0; m < MN; ++m)
-                        if (m < p.M) __stcg(mine + m * 128 + r, __uint_as_float(v[m]));
+                        if (m < p.M) ptx::st_global_hint(mine + m * 128 + r, __uint_as_float(v[m]), pol_keep);
                     __threadfence();
                     ptx::named_bar_sync(1, 32 * kEpiWarps);
                     if (etid == 0) {
@@ -253,7 +258,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                                 const int64_t cc = c0 + i;
                                 const bool have = cc <= c_last;
                                 const bool in_regs = self_in_regs && cc == c;   // own piece, not published
-                                const int64_t j = have ? t - unit_begin(cc, W, G) / KB : 0;
+                                const int64_t j = have ? t - div_nonneg(unit_begin(cc, W, G), KB) : 0;
                                 const float* src =
                                     p.partials + ((cc * p.max_tiles_per_cta + j) * MN) * 128 + r;
 #pragma unroll
