@@ -100,7 +100,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // (whole warp; one elected lane issues, as in the tiled kernel)
+        {
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
@@ -111,24 +112,28 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int64_t u = u0; u < u1; ++u) {
                 const int64_t t = div_nonneg(u, KB);
                 const int32_t kx = static_cast<int32_t>((u - t * KB) * kBK);
-                if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
+                if (!wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
-                ptx::tma_load_2d_hint(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES, &tmW, full_bar(stage), kx,
-                                      static_cast<int32_t>(t * 128), pol_w);
-                ptx::tma_load_2d_hint(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES, &tmX, full_bar(stage), kx, 0, pol_x);
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    ptx::tma_load_2d_hint(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES, &tmW, full_bar(stage), kx,
+                                          static_cast<int32_t>(t * 128), pol_w);
+                    ptx::tma_load_2d_hint(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES, &tmX, full_bar(stage), kx, 0, pol_x);
+                }
+                __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             for (int i = 0; ok && i < STAGES; ++i) {
-                ok = wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
+                ok = wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        // (whole warp; one elected lane issues every tcgen05 instruction)
+        {
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
@@ -138,31 +143,36 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const int64_t seg_end = (t + 1) * KB < u1 ? (t + 1) * KB : u1;
                 const uint32_t buf = seg & 1u;
                 const uint32_t use = (seg >> 1) & 1u;
-                if (!wait_phase(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
+                if (!wait_phase_warp(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * MN;
                 for (const int64_t seg_start = u; u < seg_end; ++u) {
-                    if (!wait_phase(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
+                    if (!wait_phase_warp(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint64_t w_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_W + stage * Cfg::W_BYTES);
                     const uint64_t x_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES);
+                    if (ptx::elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
-                                        (u != seg_start || k != 0) ? 1u : 0u);
-                    ptx::mma_commit(empty_bar(stage));
+                        for (int k = 0; k < kBK / 16; ++k)
+                            ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
+                                            (u != seg_start || k != 0) ? 1u : 0u);
+                        ptx::mma_commit(empty_bar(stage));
+                    }
+                    __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit(tfull_bar(buf));
+                if (ptx::elect_one()) ptx::mma_commit(tfull_bar(buf));
+                __syncwarp();
             }
-            ptx::mma_commit(drain_bar);
+            if (ptx::elect_one()) ptx::mma_commit(drain_bar);
+            __syncwarp();
             wait_phase(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
         }
     } else {

@@ -11,13 +11,19 @@
 // CTA pair that computes one larger MMA tile together.
 //
 // Roles (kThreads = 192):
-//   warp 0, one lane   TMA producer: for every tile and K block, wait for a
+//   warp 0             TMA producer: for every tile and K block, wait for a
 //                      free stage, then load this CTA's A rows and B rows.
-//   warp 1             allocates / frees TMEM; in the leader CTA one lane
-//                      issues the MMAs (only one thread issues, as step 1 of
-//                      the chapter requires) and commits them to barriers.
+//   warp 1             allocates / frees TMEM; in the leader CTA it issues the
+//                      MMAs (one thread issues, as step 1 of the chapter
+//                      requires) and commits them to barriers.
 //   warps 2-5          epilogue: TMEM -> registers -> fp16 -> swizzled SMEM
 //                      -> TMA store, clipped at the edges of D.
+// Warps 0 and 1 run their loops with all 32 lanes and let one elected lane
+// issue each copy, MMA and commit.  The loop's values (stage addresses,
+// descriptors) are then warp-uniform, which keeps the issuing thread fast
+// enough: run by a lone lane, the MMA loop took longer per stage than the
+// tensor pipe does (measured on GB300: the pipe idled 11 % of its cycles,
+// against under 4 % this way).
 // The accumulator is double-buffered in TMEM, so the epilogue of one tile
 // runs while the MMAs of the next tile are issued.
 #pragma once
@@ -252,7 +258,9 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // The whole warp runs the loop, so its values stay warp-uniform; one
+        // elected lane issues the barrier arrivals and copies.
+        {
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
@@ -269,38 +277,44 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
                 const uint32_t stage_bytes = Cfg::A_BYTES + (piece ? Cfg::B_BYTES / p.split : Cfg::B_BYTES);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
-                                    p.timeout_ns)) {
+                    if (!wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
+                                         p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t a_dst = sbase + stage * stride;
                     const uint32_t b_dst = a_dst + Cfg::A_BYTES;
-                    if constexpr (CG == 1) {
-                        ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-                        ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, a_row);
-                        ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kb * kBK, b_row);
-                    } else {
-                        // Both CTAs' bytes complete on the leader's full barrier; the
-                        // leader announces the pair's total.
-                        const uint32_t leader_full = ptx::mapa(full_bar(stage), 0);
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
-                        ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
-                        ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kb * kBK, b_row);
+                    if (ptx::elect_one()) {
+                        if constexpr (CG == 1) {
+                            ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+                            ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, a_row);
+                            ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kb * kBK, b_row);
+                        } else {
+                            // Both CTAs' bytes complete on the leader's full barrier; the
+                            // leader announces the pair's total.
+                            const uint32_t leader_full = ptx::mapa(full_bar(stage), 0);
+                            if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
+                            ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
+                            ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kb * kBK, b_row);
+                        }
                     }
+                    __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
             // Do not leave while an MMA commit may still arrive on this CTA's
             // barriers: wait until the MMA has released every stage.
             for (int i = 0; ok && i < STAGES; ++i) {
-                ok = wait_phase(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
+                ok = wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerTail, p.timeout_ns);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        if (rank == 0 && lane == 0) {
+        // The whole warp runs the loop, so every value it computes is
+        // warp-uniform; one elected lane (always the same one: the warp is
+        // converged) issues each tcgen05 instruction.
+        if (rank == 0) {
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
@@ -312,42 +326,44 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t idesc = ptx::idesc_kind_f16(Cfg::BM, nw, Elem<T>::kFormat);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
-                // the epilogue must have drained this accumulator buffer
-                if (!wait_phase(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
+                if (!wait_phase_warp(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
+                    if (!wait_phase_warp(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + stage * stride);
                     const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + stage * stride + Cfg::A_BYTES);
+                    if (ptx::elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // +32 bytes (2 in the >>4 address field) per 16-wide K step;
-                        // the first product of a tile overwrites the accumulator.
-                        ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                         (kb != kb0 || k != 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k)
+                            ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                                             (kb != kb0 || k != 0) ? 1u : 0u);
+                        if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
+                        else ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     }
-                    // release the stage to the producers once these MMAs have read it
-                    if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
-                    else ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                    __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                // accumulator of this tile complete: hand it to the epilogues
-                if constexpr (CG == 1) ptx::mma_commit(tfull_bar(buf));
-                else ptx::mma_commit_pair(tfull_bar(buf), 0x3);
+                if (ptx::elect_one()) {
+                    if constexpr (CG == 1) ptx::mma_commit(tfull_bar(buf));
+                    else ptx::mma_commit_pair(tfull_bar(buf), 0x3);
+                }
+                __syncwarp();
             }
-            // every MMA this thread issued has finished before TMEM is freed
-            if constexpr (CG == 1) ptx::mma_commit(drain_bar);
-            else ptx::mma_commit_pair(drain_bar, 0x1);
-            wait_phase(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
+            if (ptx::elect_one()) {
+                if constexpr (CG == 1) ptx::mma_commit(drain_bar);
+                else ptx::mma_commit_pair(drain_bar, 0x1);
+            }
+            __syncwarp();
+            wait_phase_warp(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
         }
     } else {
         // ------------------------------------------------------------ epilogue
