@@ -70,6 +70,22 @@ def dist_env():
 
 
 # ---------------------------------------------------------------- host-side helpers
+def max_over_ranks(pg, x: float, device) -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself with one rank."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, M: int, N: int, K: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank ran one M x N x K product per step (replicas),
+    timed by the slowest rank."""
+    return world * metrics.tflops(M, N, K, ms_max * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -371,14 +387,11 @@ def run_ours(args):
     region_ms = ev0.elapsed_time(ev1)
     ms_per_step = region_ms / args.steps
     launch_ms = ms_per_step          # average launch duration over the timed region (this rank)
-    if pg:
-        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(pg, ms_per_step, dev)
     if sampler:
         sampler.mark(t_wall0, t_wall1)
 
-    value = world * metrics.tflops(w.M, w.N, w.K, ms_per_step * 1e-3)
+    value = job_tflops(world, w.M, w.N, w.K, ms_per_step)
 
     # end to end through the C ABI: pinned host operands in, pinned host result out
     e2e = None
@@ -410,12 +423,9 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if pg:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(pg, e2e_ms, dev)
         g.gemm_f16_nt_check(stream=stream, device=dev)
-        e2e = {"value": world * metrics.tflops(w.M, w.N, w.K, e2e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": job_tflops(world, w.M, w.N, w.K, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(src.numel() * 2 for _, src in host_in),
                "d2h_bytes_per_step": D_pin.numel() * 2}
