@@ -264,10 +264,16 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             int stage = 0;
             uint32_t phase = 0;
-            for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters) {
+            uint32_t round = 0;
+            for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters, ++round) {
                 int64_t tm, n0;
                 int nw, kb0, kb1;
                 work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
+                // Odd rounds walk K downwards: a round starts on the K blocks the
+                // previous round (on the same tile rows) read last, which are the
+                // ones still in L2.  Only the load order changes (the MMA takes
+                // stages as they come); split-K pieces keep one direction.
+                const bool reverse = (round & 1u) && p.ksplit == 1;
                 // each CTA of a pair supplies nw / CG rows of B to the MMA; a
                 // column piece of a tail tile loads only those rows (box of the
                 // second B map) instead of the whole tile's
@@ -284,18 +290,19 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                     const uint32_t a_dst = sbase + stage * stride;
                     const uint32_t b_dst = a_dst + Cfg::A_BYTES;
+                    const int kx = (reverse ? (kb1 - 1 - (kb - kb0)) : kb) * kBK;
                     if (ptx::elect_one()) {
                         if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-                            ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, a_row);
-                            ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kb * kBK, b_row);
+                            ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kx, a_row);
+                            ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kx, b_row);
                         } else {
                             // Both CTAs' bytes complete on the leader's full barrier; the
                             // leader announces the pair's total.
                             const uint32_t leader_full = ptx::mapa(full_bar(stage), 0);
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
-                            ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kb * kBK, a_row);
-                            ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kb * kBK, b_row);
+                            ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kx, a_row);
+                            ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kx, b_row);
                         }
                     }
                     __syncwarp();

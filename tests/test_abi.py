@@ -144,7 +144,8 @@ def test_plans_for_the_named_workloads(lib):
     # 1024 tiles on 76 pairs: 13 whole rounds (988 tiles), the last 36 tiles cut
     # in halves (72 pieces on 76 pairs) instead of a 14th round of 36 tiles
     assert (p["num_full_tiles"], p["tail_split"]) == (988, 2)
-    assert p["group_m"] == 8                 # 8 x 256 rows x 16 KB = 32 MiB of A per group (34 MiB budget)
+    # at most 12 tile rows (12 x 256 rows x 16 KB = 48 MiB of A) per group: 32 rows in 3 groups of 11
+    assert p["group_m"] == 11
     p = P(4000, 11000, 4104)
     assert p["variant"] == "TILE_2CTA_256x256"
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)   # ragged in M, N and K
