@@ -234,12 +234,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
                 if (owner) ptx::named_bar_sync(1, 32 * kEpiWarps);
                 if (!(owner && *last_flag == 2u)) {
-                    float* mine = p.partials +
-                                  ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128;
+                    // a piece's partial is [MN / 4][128 rows][4] fp32: a thread (row r)
+                    // moves four consecutive columns with one 16-byte access, and the
+                    // 32 lanes of a warp cover one contiguous 512-byte run
+                    float4* mine = reinterpret_cast<float4*>(
+                                       p.partials + ((c * p.max_tiles_per_cta + (t - first_tile)) * MN) * 128) + r;
                     const uint64_t pol_keep = ptx::policy_evict_last();   // read back soon by the reducer
 #pragma unroll
-                    for (int m = 0; m < MN; ++m)
-                        if (m < p.M) ptx::st_global_hint(mine + m * 128 + r, __uint_as_float(v[m]), pol_keep);
+                    for (int q = 0; q < MN / 4; ++q)
+                        ptx::st_global_hint_v4(mine + q * 128,
+                                               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])),
+                                               pol_keep);
                     __threadfence();
                     ptx::named_bar_sync(1, 32 * kEpiWarps);
                     if (etid == 0) {
@@ -255,33 +261,43 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         EpiColumn<T, MN> ec;
                         if (p.epi.on) ec.load(p.epi, n, p.M, p.N);   // in flight during the sum
                         // Sum the pieces in ascending CTA order.  Pieces are fetched
-                        // CH at a time with independent loads so their latencies
-                        // overlap; the additions keep the fixed order.
+                        // CH at a time, every 16-byte load of a batch issued before
+                        // any of them is used, so their latencies overlap; the
+                        // additions keep the fixed order.
                         constexpr int CH = 64 / MN;
                         float acc[MN];
 #pragma unroll
                         for (int m = 0; m < MN; ++m) acc[m] = 0.0f;
                         for (int64_t c0 = c_first; c0 <= c_last; c0 += CH) {
-                            float pv[CH][MN];
+                            float4 pv[CH][MN / 4];
 #pragma unroll
                             for (int i = 0; i < CH; ++i) {
                                 const int64_t cc = c0 + i;
-                                const bool have = cc <= c_last;
-                                const bool in_regs = self_in_regs && cc == c;   // own piece, not published
-                                const int64_t j = have ? t - div_nonneg(unit_begin(cc, W, G), KB) : 0;
-                                const float* src =
-                                    p.partials + ((cc * p.max_tiles_per_cta + j) * MN) * 128 + r;
+                                const bool load = cc <= c_last && !(self_in_regs && cc == c);
+                                const int64_t j = load ? t - div_nonneg(unit_begin(cc, W, G), KB) : 0;
+                                const float4* src = reinterpret_cast<const float4*>(
+                                                        p.partials + ((cc * p.max_tiles_per_cta + j) * MN) * 128) + r;
 #pragma unroll
-                                for (int m = 0; m < MN; ++m)
-                                    pv[i][m] = in_regs ? __uint_as_float(v[m])
-                                               : (have && m < p.M) ? __ldcg(src + m * 128) : 0.0f;
+                                for (int q = 0; q < MN / 4; ++q)
+                                    pv[i][q] = load ? __ldcg(src + q * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
-                            for (int i = 0; i < CH; ++i)
-                                if (c0 + i <= c_last) {
+                            for (int i = 0; i < CH; ++i) {
+                                const int64_t cc = c0 + i;
+                                if (cc > c_last) continue;
+                                if (self_in_regs && cc == c) {   // own piece, still in registers
 #pragma unroll
-                                    for (int m = 0; m < MN; ++m) acc[m] += pv[i][m];
+                                    for (int m = 0; m < MN; ++m) acc[m] += __uint_as_float(v[m]);
+                                } else {
+#pragma unroll
+                                    for (int q = 0; q < MN / 4; ++q) {
+                                        acc[4 * q] += pv[i][q].x;
+                                        acc[4 * q + 1] += pv[i][q].y;
+                                        acc[4 * q + 2] += pv[i][q].z;
+                                        acc[4 * q + 3] += pv[i][q].w;
+                                    }
                                 }
+                            }
                         }
 #pragma unroll
                         for (int m = 0; m < MN; ++m) {

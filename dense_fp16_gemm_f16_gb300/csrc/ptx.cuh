@@ -127,6 +127,12 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "l"(policy) : "memory");
 }
 
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_hint_v4(float4* addr, float4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+                 :: "l"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy) : "memory");
+}
+
 // 32-bit global store with an L2 cache policy.
 __device__ __forceinline__ void st_global_hint(float* addr, float v, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" :: "l"(addr), "f"(v), "l"(policy) : "memory");
