@@ -36,6 +36,7 @@ struct DeviceState {
     int sms = 0;
     uint32_t* status = nullptr;
     int max_clusters_2cta = 0;   // co-resident 2-CTA clusters of the 256x256 kernel
+    int max_clusters_4cta = 0;   // co-resident 4-CTA clusters of the 512x256 kernel
     int per_sm_1cta128 = 0;      // co-resident CTAs per SM
     int per_sm_1cta256 = 0;
 };
@@ -89,18 +90,29 @@ gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K) {
 struct Limits {
     int sms;
     int max_clusters_2cta;
+    int max_clusters_4cta;
     int per_sm_1cta128;
     int per_sm_1cta256;
 };
 
 int skinny_mn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// The ops table of a tiled variant.
+const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
+    switch (v) {
+        case GEMM_VARIANT_TILE_1CTA_128x128: return tiled_ops_1cta128(dtype);
+        case GEMM_VARIANT_TILE_1CTA_128x256: return tiled_ops_1cta256(dtype);
+        case GEMM_VARIANT_TILE_4CTA_512x256: return tiled_ops_4cta512(dtype);
+        default: return tiled_ops_2cta256(dtype);   // TILE_2CTA_256x256, TILE_2CTA_SPLITK
+    }
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant, const Limits& lim,
                         gemm_plan_t* pl) {
     std::memset(pl, 0, sizeof(*pl));
     const gemm_status_t st = check_sizes(M, N, K);
     if (st != GEMM_OK) return st;
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
     const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
@@ -122,7 +134,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // (measured on GB300: 512x2048x8192 22.9 us split vs 39.1 us on
             // 128x256 tiles; 1024x1024x2048 15.8 us split vs 12.7 us).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
-            if (t2 >= pairs) variant = GEMM_VARIANT_TILE_2CTA_256x256;
+            // When K is not a multiple of 16 the rows of A and B do not start on
+            // 32-byte sectors, so every 128-byte TMA row reads five sectors
+            // instead of four; then the 4-CTA clusters, which fetch each B block
+            // once for two pairs, win despite using 144 of the 152 SMs (measured
+            // on GB300: 4000x11000x4104 226 us against 253 us on pairs, K = 4136
+            // 220 against 252; with sector-aligned rows pairs are faster or
+            // level: 8192^3 641 against 656 us, K = 4112 207 against 212).
+            if (t2 >= pairs) variant = (K % 16 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
             else if (cdiv(K, kBK) >= kSplitKMinBlocks && choose_ksplit(t2, pairs, cdiv(K, kBK)) > 1)
                 variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
             else if (cdiv(M, 128) * cdiv(N, 256) >= 2) variant = GEMM_VARIANT_TILE_1CTA_128x256;
@@ -164,9 +183,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
         variant = GEMM_VARIANT_TILE_2CTA_256x256;   // enough tiles already: no split
     pl->variant = variant;
     const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK;
-    const TiledOps& ops = (variant == GEMM_VARIANT_TILE_2CTA_256x256 || ksplit_variant) ? tiled_ops_2cta256(0)
-                          : variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128(0)
-                                                                      : tiled_ops_1cta256(0);
+    const TiledOps& ops = tiled_ops_of(variant, 0);
     pl->cta_group = ops.cta_group;
     pl->tile_m = ops.tile_m;
     pl->tile_n = ops.tile_n;
@@ -177,9 +194,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     pl->n_tiles = cdiv(N, ops.tile_n);
     if (M == 0 || N == 0 || K == 0) return GEMM_OK;
     const int64_t tiles = pl->m_tiles * pl->n_tiles;
-    // slots = CTA pairs (or CTAs) that can be resident at once
+    // slots = clusters (or CTAs) that can be resident at once
     int64_t slots;
-    if (ops.cta_group == 2) {
+    if (ops.cluster == 4) {
+        slots = lim.max_clusters_4cta > 0 ? lim.max_clusters_4cta : lim.sms / 4;
+    } else if (ops.cta_group == 2) {
         slots = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
     } else {
         const int per_sm = variant == GEMM_VARIANT_TILE_1CTA_128x128 ? lim.per_sm_1cta128 : lim.per_sm_1cta256;
@@ -200,7 +219,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     pl->k_split = ksplit;
     const int64_t units = ksplit > 1 ? tiles * ksplit : num_full + (tiles - num_full) * split;
     const int64_t clusters = units < slots ? units : slots;
-    pl->grid_ctas = static_cast<int32_t>(clusters * ops.cta_group);
+    pl->grid_ctas = static_cast<int32_t>(clusters * ops.cluster);
     pl->num_full_tiles = num_full;
     pl->tail_split = split;
     pl->group_m = static_cast<int32_t>(raster_group(pl->m_tiles, ops.tile_m, K));
@@ -247,21 +266,24 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
         }
         const TiledOps* tiled[3] = {&tiled_ops_2cta256(0), &tiled_ops_1cta128(0), &tiled_ops_1cta256(0)};
         for (int dt : {0, 1}) {
-            const TiledOps* all[3] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt)};
+            const TiledOps* all[4] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt),
+                                      &tiled_ops_4cta512(dt)};
             for (const TiledOps* t : all)
                 if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
             for (int mn : {16, 32, 64})
                 if (skinny_ops(mn, dt).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
         }
         int clusters = 0, per128 = 0, per256 = 0;
+        int clusters4 = 0;
         if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
-            tiled[2]->max_active(&per256) != cudaSuccess) {
+            tiled[2]->max_active(&per256) != cudaSuccess || tiled_ops_4cta512(0).max_active(&clusters4) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         d.sms = sms;
         d.status = static_cast<uint32_t*>(status);
         d.max_clusters_2cta = clusters;
+        d.max_clusters_4cta = clusters4;
         d.per_sm_1cta128 = per128;
         d.per_sm_1cta256 = per256;
         d.ready = true;
@@ -272,7 +294,7 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    return Limits{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256};
+    return Limits{d.sms, d.max_clusters_2cta, d.max_clusters_4cta, d.per_sm_1cta128, d.per_sm_1cta256};
 }
 
 // 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
@@ -395,7 +417,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
             if (epi.bias && ranges_overlap(epi.bias, N * 2, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
@@ -465,10 +487,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         return GEMM_OK;
     }
 
-    const TiledOps& ops = (pl.variant == GEMM_VARIANT_TILE_2CTA_256x256 || pl.variant == GEMM_VARIANT_TILE_2CTA_SPLITK)
-                              ? tiled_ops_2cta256(dtype)
-                          : pl.variant == GEMM_VARIANT_TILE_1CTA_128x128 ? tiled_ops_1cta128(dtype)
-                                                                         : tiled_ops_1cta256(dtype);
+    const TiledOps& ops = tiled_ops_of(static_cast<gemm_variant_t>(pl.variant), dtype);
     Workspace* ws = nullptr;
     if (pl.k_split > 1) {
         const size_t partial_bytes = static_cast<size_t>(pl.m_tiles * pl.n_tiles) * pl.k_split * ops.tile_m *
@@ -477,7 +496,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         if (st != GEMM_OK) return st;
     }
     CUtensorMap ta, tb, tbp, td;
-    const uint32_t b_rows = static_cast<uint32_t>(ops.tile_n / ops.cta_group);
+    const uint32_t b_rows = static_cast<uint32_t>(ops.b_box_rows);
     if (!encode_2d(&ta, A, K, M, kBK, 128, dtype) || !encode_2d(&tb, B, K, N, kBK, b_rows, dtype) ||
         !encode_2d(&tbp, B, K, N, kBK, b_rows / static_cast<uint32_t>(pl.tail_split), dtype) ||
         !encode_2d(&td, D, N, M, 64, 32, dtype))
@@ -681,7 +700,7 @@ GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_va
     if (plan == nullptr) return GEMM_ERR_INVALID_VALUE;
     Limits lim;
     if (num_sms > 0) {
-        lim = Limits{num_sms, num_sms / 2, 1, 1};
+        lim = Limits{num_sms, num_sms / 2, num_sms / 4, 1, 1};
     } else {
         DeviceState* dev = nullptr;
         const gemm_status_t st = get_device(&dev, nullptr);

@@ -11,7 +11,10 @@
 namespace gemm_gb300 {
 
 struct TiledOps {
-    int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols;
+    // tile_m: rows of one unit of work (a cluster tile); cluster: CTAs per cluster;
+    // b_box_rows: rows of B per TMA box (each CTA's B rows, or half of them when
+    // two pairs share B)
+    int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols, cluster, b_box_rows;
     // set the kernel's shared-memory limit on the current device
     cudaError_t (*prepare)();
     // co-resident clusters (cta_group 2) or CTAs per SM (cta_group 1) on the current device
@@ -31,6 +34,7 @@ struct SkinnyOps {
 
 // dtype: 0 = fp16 operands and output, 1 = bf16
 const TiledOps& tiled_ops_2cta256(int dtype);
+const TiledOps& tiled_ops_4cta512(int dtype);
 const TiledOps& tiled_ops_1cta128(int dtype);
 const TiledOps& tiled_ops_1cta256(int dtype);
 const SkinnyOps& skinny_ops(int mn, int dtype);  // mn = 16, 32 or 64

@@ -147,10 +147,14 @@ def test_plans_for_the_named_workloads(lib):
     # at most 12 tile rows (12 x 256 rows x 16 KB = 48 MiB of A) per group: 32 rows in 3 groups of 11
     assert p["group_m"] == 11
     p = P(4000, 11000, 4104)
-    assert p["variant"] == "TILE_2CTA_256x256"
-    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)   # ragged in M, N and K
-    assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds + 4 tiles in quarters
-    assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
+    # K = 4104 is not a multiple of 64 (rows not on 128-byte lines): 4-CTA
+    # clusters of two pairs sharing B, 512 x 256 per cluster
+    assert p["variant"] == "TILE_4CTA_512x256" and p["grid_ctas"] % 4 == 0
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (8, 43, 65)    # ragged in M, N and K
+    assert (p["num_full_tiles"], p["tail_split"]) == (342, 4)           # 9 rounds of 38 + 2 tiles in quarters
+    assert p["group_m"] == 8                                            # all of A (32 MiB) in one group
+    q = P(4000, 11000, 4104, variant=g.Variant.TILE_2CTA_256x256)       # the pair kernel on request
+    assert (q["m_tiles"], q["num_full_tiles"], q["tail_split"]) == (16, 684, 4)
     p = P(1024, 1024, 2048)
     # 16 pair tiles but a short K loop (32 blocks): 128x256 tiles in quarters
     assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1
