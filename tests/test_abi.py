@@ -153,6 +153,9 @@ def test_plans_for_the_named_workloads(lib):
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (8, 43, 65)    # ragged in M, N and K
     assert (p["num_full_tiles"], p["tail_split"]) == (342, 4)           # 9 rounds of 38 + 2 tiles in quarters
     assert p["group_m"] == 8                                            # all of A (32 MiB) in one group
+    # rows on 32-byte sectors (K a multiple of 16): the pair kernel, on all 152 SMs
+    assert P(4000, 11000, 4112)["variant"] == "TILE_2CTA_256x256"
+    assert P(4000, 11000, 4136)["variant"] == "TILE_4CTA_512x256"
     q = P(4000, 11000, 4104, variant=g.Variant.TILE_2CTA_256x256)       # the pair kernel on request
     assert (q["m_tiles"], q["num_full_tiles"], q["tail_split"]) == (16, 684, 4)
     p = P(1024, 1024, 2048)
