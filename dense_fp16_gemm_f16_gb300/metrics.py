@@ -1,4 +1,4 @@
-"""Throughput figures the GEMM is judged by.
+"""Throughput figures reported for the GEMM.
 
 TFLOPS counts one multiply-add as two floating-point operations:
 TFLOPS = 2·M·N·K / (t · 10¹²) -- "Building a Tiled GEMM" (MLC), section
