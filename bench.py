@@ -387,7 +387,11 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    gbuild.build()
+    # one process builds (ranks would otherwise race on the same output files)
+    if local_rank == 0:
+        gbuild.build()
+    if pg:
+        pg.barrier()
     g.load()
     w = workload_of(args)
     A_h, B_h = operands_of(w, args.dtype)
