@@ -412,7 +412,7 @@ def run_ours(args):
     # Operands smaller than twice the L2 are rotated over enough copies that
     # consecutive launches never find them in L2 (no flush needed between them).
     ab_bytes = (w.M * w.K + w.N * w.K) * 2
-    copies = 1 if ab_bytes >= L2_ROTATE_BYTES else min(64, -(-L2_ROTATE_BYTES // max(ab_bytes, 1)))
+    copies = 1 if ab_bytes >= L2_ROTATE_BYTES else max(4, min(64, -(-L2_ROTATE_BYTES // max(ab_bytes, 1))))
     As, Bs = [A], [B]
     for _ in range(copies - 1):
         As.append(A.clone())
@@ -479,6 +479,24 @@ def run_ours(args):
     if sampler:
         sampler.mark(t_wall0, t_wall1)
 
+    # Spread of the per-launch time: after the timed region, the same launches
+    # in (up to) 30 batches with an event pair around each; reported beside the
+    # value, which stays the one-region measurement above.
+    batches = min(30, args.steps)
+    per_batch = max(1, args.steps // batches)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(batches + 1)]
+    evs[0].record(stream)
+    for b in range(batches):
+        for _ in range(per_batch):
+            step()
+        evs[b + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    g.gemm_f16_nt_check(stream=stream, device=dev)
+    per_launch = sorted(evs[b].elapsed_time(evs[b + 1]) / per_batch for b in range(batches))
+    spread = {"batches": batches, "launches_per_batch": per_batch,
+              "median_ms": statistics.median(per_launch), "min_ms": per_launch[0],
+              "p90_ms": per_launch[min(batches - 1, int(0.9 * batches))]}
+
     value = job_tflops(world, w.M, w.N, w.K, ms_per_step)
 
     # end to end through the C ABI: pinned host operands in, pinned host result out
@@ -539,6 +557,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
+        "per_launch_spread": spread,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
