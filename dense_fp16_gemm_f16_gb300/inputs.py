@@ -137,12 +137,8 @@ def sample_entries(M: int, N: int, seed: int, n_rows: int = 8, n_cols: int = 8,
     return np.concatenate(r_parts), np.concatenate(c_parts)
 
 
-def draw_bf16(rows: int, cols: int, dist: str, seed: int, K: int | None = None) -> np.ndarray:
-    """bf16 operands as uint16 bit patterns: the same float64 draws as ``draw``,
-    rounded to float32 and then to bf16 by torch (nearest, ties to even).  Any
-    bf16 value is a valid input; the CPU oracle and the GPU see the same bits."""
-    import torch
-
+def _draw_f64(rows: int, cols: int, dist: str, seed: int, K: int | None = None) -> np.ndarray:
+    """The float64 draws behind ``draw`` (one generator call), as [rows, cols]."""
     K = cols if K is None else K
     rng = np.random.default_rng(seed)
     n = rows * cols
@@ -152,8 +148,66 @@ def draw_bf16(rows: int, cols: int, dist: str, seed: int, K: int | None = None) 
         x = rng.normal(0.0, _sigma(dist, K), n)
     else:
         raise ValueError(f"unknown distribution {dist!r}")
+    return x.reshape(rows, cols)
+
+
+def draw_bf16(rows: int, cols: int, dist: str, seed: int, K: int | None = None) -> np.ndarray:
+    """bf16 operands as uint16 bit patterns: the same float64 draws as ``draw``,
+    rounded to float32 and then to bf16 by torch (nearest, ties to even).  Any
+    bf16 value is a valid input; the CPU oracle and the GPU see the same bits."""
+    import torch
+
+    x = _draw_f64(rows, cols, dist, seed, K).ravel()
     t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16).reshape(rows, cols).copy()
+
+
+#: largest finite value of each 8-bit operand type
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def _torch_fp8(fmt: str):
+    import torch
+    if fmt == "e4m3":
+        return torch.float8_e4m3fn
+    if fmt == "e5m2":
+        return torch.float8_e5m2
+    raise ValueError(f"unknown 8-bit format {fmt!r}")
+
+
+def draw_fp8(rows: int, cols: int, dist: str, seed: int, fmt: str = "e4m3", K: int | None = None,
+             per_row: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """8-bit operands with their fp32 scales: the same float64 draws as ``draw``,
+    divided by a scale that maps their largest magnitude onto the format's
+    largest finite value -- one scale for the whole array, or one per row when
+    ``per_row`` -- and rounded by torch's float32 -> 8-bit conversion (nearest,
+    ties to even).  This is the amax scaling of the GEMM blog post's
+    quantisation step (section 4.2); values times scale approximate the draws.
+    Returns (bits uint8 [rows, cols], scale float32 [rows] or [1]).  Any
+    finite 8-bit value is a valid input: the CPU oracle and the GPU see the
+    same bits and the same scales."""
+    import torch
+
+    x = _draw_f64(rows, cols, dist, seed, K)
+    top = FP8_MAX[fmt]
+    amax = np.abs(x).max(axis=1) if per_row else np.array([np.abs(x).max() if x.size else 0.0])
+    scale = (amax / top).astype(np.float32)
+    scale[scale == 0] = 1.0
+    div = scale.astype(np.float64)[:, None] if per_row else np.float64(scale[0])
+    q = torch.from_numpy((x / div).astype(np.float32)).clamp_(-top, top).to(_torch_fp8(fmt))
+    return q.view(torch.uint8).numpy().copy(), scale
+
+
+def operands_fp8(M: int, N: int, K: int, dist_a: str = "uniform", dist_b: str = "uniform", seed: int = 0,
+                 fmt: str = "e4m3") -> tuple[np.ndarray, np.ndarray, float, np.ndarray]:
+    """(A [M,K], B [N,K], a_scale, b_scale [N]) for the 8-bit GEMM: A (the
+    activations) from ``seed`` with one scale, B (the weights, one output
+    channel per row) from ``seed + 1000`` with one scale per row.  With D's
+    fused transform ``alpha = a_scale`` and per-column scale ``b_scale`` the
+    GEMM computes the dequantised product."""
+    A, sa = draw_fp8(M, K, dist_a, seed, fmt, K=K)
+    B, sb = draw_fp8(N, K, dist_b, seed + 1000, fmt, K=K, per_row=True)
+    return A, B, float(sa[0]), sb
 
 
 def operands_bf16(M: int, N: int, K: int, dist_a: str = "uniform", dist_b: str = "uniform",

@@ -15,9 +15,12 @@ loads it and marshals numpy arrays.
 Pins (tests/test_oracle.py): the fp16 decode/encode is checked exhaustively
 and against numpy's own float64→float16 routine; the GEMM against exact int64
 arithmetic on small-integer inputs, and against closed forms (all-ones,
-identity B, rank-1, zero blocks).  Every function here is pinned, and the
-tests also build broken copies of the C file to show that each pin fails
-when a plausible mistake is planted.
+identity B, rank-1, zero blocks).  The bf16 and 8-bit (E4M3, E5M2) decoders
+are checked exhaustively against torch's conversions (tests/test_oracle_ex.py,
+tests/test_oracle_fp8.py), the fused transform and the per-column scale
+against exact arithmetic.  Every function here is pinned, and the tests also
+build broken copies of the C file to show that each pin fails when a
+plausible mistake is planted.
 """
 from __future__ import annotations
 
@@ -97,8 +100,12 @@ class Oracle:
         lib.oracle_f64_to_bf16.argtypes = [p, p, i64]
         lib.oracle_f64_to_bf16.restype = None
         d = ctypes.c_double
+        lib.oracle_e4m3_to_f64.argtypes = [p, p, i64]
+        lib.oracle_e4m3_to_f64.restype = None
+        lib.oracle_e5m2_to_f64.argtypes = [p, p, i64]
+        lib.oracle_e5m2_to_f64.restype = None
         lib.oracle_gemm_nt_ex.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p, i64, i64, i64,
-                                          d, d, p, p, ctypes.c_int, p, p, ctypes.c_int]
+                                          d, d, p, p, p, ctypes.c_int, p, p, ctypes.c_int]
         lib.oracle_gemm_nt_ex.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -132,6 +139,20 @@ class Oracle:
         a = np.ascontiguousarray(x, dtype=np.float64)
         out = np.empty(a.shape, dtype=np.uint16)
         self.lib.oracle_f64_to_bf16(_ptr(a), _ptr(out), a.size)
+        return out
+
+    def e4m3_to_f64(self, bits) -> np.ndarray:
+        """Decode E4M3 bit patterns (uint8) into float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_e4m3_to_f64(_ptr(b), _ptr(out), b.size)
+        return out
+
+    def e5m2_to_f64(self, bits) -> np.ndarray:
+        """Decode E5M2 bit patterns (uint8) into float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_e5m2_to_f64(_ptr(b), _ptr(out), b.size)
         return out
 
     # -- the GEMM -------------------------------------------------------------
@@ -215,25 +236,38 @@ def gemm(A, B, nthreads=None, want_sums=False):
 
 
 # ---------------------------------------------------------------------------
-# element type + fused epilogue:  D = round(act(alpha * A Bᵀ + beta * C + bias[n]))
+# element type + fused epilogue:
+#   D = round(act(alpha * scale_n[n] * A Bᵀ + beta * C + bias[n]))
 # ---------------------------------------------------------------------------
-DTYPES = {"f16": 0, "bf16": 1}
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}
+#: 8-bit operand types; their D, C and bias are bf16
+FP8 = ("e4m3", "e5m2")
+
+
+def out_dtype(dtype: str) -> str:
+    """Element type of D (and C, bias) for an operand type."""
+    return "f16" if dtype == "f16" else "bf16"
 
 
 def _bits(x, dtype: str) -> np.ndarray:
-    """uint16 bit patterns of an operand: float16 arrays for f16, uint16 for bf16."""
+    """Bit patterns of an array: float16 arrays for f16, uint16 for bf16,
+    uint8 for the 8-bit types."""
     a = np.ascontiguousarray(x)
     if dtype == "f16":
         if a.dtype != np.float16:
             raise TypeError(f"f16 operands must be float16 arrays, got {a.dtype}")
         return a.view(np.uint16)
+    if dtype in FP8:
+        if a.dtype != np.uint8:
+            raise TypeError(f"{dtype} operands must be uint8 bit-pattern arrays, got {a.dtype}")
+        return a
     if a.dtype != np.uint16:
         raise TypeError(f"bf16 operands must be uint16 bit-pattern arrays, got {a.dtype}")
     return a
 
 
 def _gemm_ex(o: Oracle, A, B, dtype, alpha, beta, C, bias, relu, rows=None, cols=None,
-             row_begin=0, row_end=None, nthreads=None, want_pre=False):
+             row_begin=0, row_end=None, nthreads=None, want_pre=False, scale_n=None):
     if dtype not in DTYPES:
         raise ValueError(f"dtype must be one of {sorted(DTYPES)}")
     Ab, Bb = _bits(A, dtype), _bits(B, dtype)
@@ -241,12 +275,18 @@ def _gemm_ex(o: Oracle, A, B, dtype, alpha, beta, C, bias, relu, rows=None, cols
         raise ValueError("need A [M,K] and B [N,K]")
     M, K = Ab.shape
     N = Bb.shape[0]
-    Cb = None if C is None or beta == 0 else _bits(C, dtype)
+    od = out_dtype(dtype)
+    Cb = None if C is None or beta == 0 else _bits(C, od)
     if Cb is not None and Cb.shape != (M, N):
         raise ValueError("C must be [M, N]")
-    biasb = None if bias is None else _bits(bias, dtype)
+    biasb = None if bias is None else _bits(bias, od)
     if biasb is not None and biasb.shape != (N,):
         raise ValueError("bias must be [N]")
+    sc = None
+    if scale_n is not None:
+        sc = np.ascontiguousarray(scale_n)
+        if sc.dtype != np.float32 or sc.shape != (N,):
+            raise TypeError("scale_n must be a float32 [N] array")
     if rows is not None:
         r = np.ascontiguousarray(rows, dtype=np.int64).ravel()
         c = np.ascontiguousarray(cols, dtype=np.int64).ravel()
@@ -261,26 +301,26 @@ def _gemm_ex(o: Oracle, A, B, dtype, alpha, beta, C, bias, relu, rows=None, cols
     out = np.empty(shape, dtype=np.uint16)
     pre = np.empty(shape, dtype=np.float64) if want_pre else None
     rc = o.lib.oracle_gemm_nt_ex(DTYPES[dtype], _ptr(Ab), _ptr(Bb), M, N, K, rp, cp, count, rb, re,
-                                 float(alpha), float(beta), _ptr(Cb), _ptr(biasb), 1 if relu else 0,
-                                 _ptr(pre), _ptr(out), nthreads or default_threads())
+                                 float(alpha), float(beta), _ptr(Cb), _ptr(biasb), _ptr(sc),
+                                 1 if relu else 0, _ptr(pre), _ptr(out), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle_gemm_nt_ex rejected its arguments")
-    res = out.view(np.float16) if dtype == "f16" else out
+    res = out.view(np.float16) if od == "f16" else out
     return (res, pre) if want_pre else res
 
 
 def gemm_ex(A, B, dtype="f16", alpha=1.0, beta=0.0, C=None, bias=None, relu=False,
-            nthreads=None, want_pre=False, oracle=None):
-    """Whole D (float16 for f16, uint16 bf16 bit patterns for bf16)."""
+            nthreads=None, want_pre=False, oracle=None, scale_n=None):
+    """Whole D (float16 for f16, uint16 bf16 bit patterns otherwise)."""
     return _gemm_ex(oracle or default(), A, B, dtype, alpha, beta, C, bias, relu,
-                    nthreads=nthreads, want_pre=want_pre)
+                    nthreads=nthreads, want_pre=want_pre, scale_n=scale_n)
 
 
 def gemm_ex_entries(A, B, rows, cols, dtype="f16", alpha=1.0, beta=0.0, C=None, bias=None, relu=False,
-                    nthreads=None, oracle=None):
+                    nthreads=None, oracle=None, scale_n=None):
     """D at the listed (row, col) entries."""
     return _gemm_ex(oracle or default(), A, B, dtype, alpha, beta, C, bias, relu, rows=rows, cols=cols,
-                    nthreads=nthreads)
+                    nthreads=nthreads, scale_n=scale_n)
 
 
 def bf16_to_f64(bits):
@@ -289,3 +329,11 @@ def bf16_to_f64(bits):
 
 def f64_to_bf16(x):
     return default().f64_to_bf16(x)
+
+
+def e4m3_to_f64(bits):
+    return default().e4m3_to_f64(bits)
+
+
+def e5m2_to_f64(bits):
+    return default().e5m2_to_f64(bits)

@@ -156,6 +156,48 @@ static uint16_t bf16_encode(double x) {
     return sign | (uint16_t)(expo << 7) | (uint16_t)(n - 128);
 }
 
+/* ------------------------------------------------------------------ */
+/* 8-bit floating point: the GEMM blog post (section 2.2) lists FP8 in  */
+/* two layouts, E4M3 and E5M2.  The encodings are those of the 8-bit    */
+/* formats that the tensor cores take (the OCP 8-bit floating point     */
+/* formats):                                                            */
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits, no      */
+/*   infinities; S.1111.111 is the only NaN.                            */
+/*   exponent field 0     : subnormal, value = frac * 2^-9              */
+/*   exponent field 1..15 : normal,    value = (8 + frac) * 2^(e - 10)  */
+/*   Largest finite: S.1111.110 = 14 * 2^5 = 448, the bound the blog    */
+/*   post's quantisation step (section 4.2) scales values to.           */
+/* E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, laid   */
+/*   out like binary16 with 8 fewer fraction bits.                      */
+/*   exponent field 0     : subnormal, value = frac * 2^-16             */
+/*   exponent field 1..30 : normal,    value = (4 + frac) * 2^(e - 17)  */
+/*   exponent field 31    : infinity (frac == 0) or NaN.                */
+/*   Largest finite: 7 * 2^13 = 57344.                                  */
+/* The product of two such values has at most 3 + 3 (or 2 + 2)          */
+/* significant bits beyond the leading one: exact in fp64.              */
+/* ------------------------------------------------------------------ */
+static double e4m3_decode(uint8_t h) {
+    const int sign = (h >> 7) & 1;
+    const int expo = (h >> 3) & 0xF;
+    const int frac = h & 0x7;
+    double v;
+    if (expo == 0) v = ldexp((double)frac, -9);
+    else if (expo == 15 && frac == 7) v = NAN;
+    else v = ldexp((double)(8 + frac), expo - 10);
+    return sign ? -v : v;
+}
+
+static double e5m2_decode(uint8_t h) {
+    const int sign = (h >> 7) & 1;
+    const int expo = (h >> 2) & 0x1F;
+    const int frac = h & 0x3;
+    double v;
+    if (expo == 0) v = ldexp((double)frac, -16);
+    else if (expo == 31) v = frac ? NAN : INFINITY;
+    else v = ldexp((double)(4 + frac), expo - 17);
+    return sign ? -v : v;
+}
+
 /* Decode table built from f16_decode, so the inner loop does not re-derive
  * each value.  Built once, thread-safely. */
 static double g_decode[65536];
@@ -178,8 +220,32 @@ static const double* decode_bf16_table(void) {
     return g_decode_bf16;
 }
 
+static double g_decode_e4m3[256], g_decode_e5m2[256];
+static pthread_once_t g_decode_f8_once = PTHREAD_ONCE_INIT;
+static void build_decode_f8_tables(void) {
+    for (uint32_t h = 0; h < 256u; ++h) {
+        g_decode_e4m3[h] = e4m3_decode((uint8_t)h);
+        g_decode_e5m2[h] = e5m2_decode((uint8_t)h);
+    }
+}
+static const double* decode_e4m3_table(void) {
+    pthread_once(&g_decode_f8_once, build_decode_f8_tables);
+    return g_decode_e4m3;
+}
+static const double* decode_e5m2_table(void) {
+    pthread_once(&g_decode_f8_once, build_decode_f8_tables);
+    return g_decode_e5m2;
+}
+
 /* One element of the definition: ascending k, one fp64 accumulator. */
 static double dot_row_row(const double* dec, const uint16_t* a_row, const uint16_t* b_row, int64_t K) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) acc += dec[a_row[k]] * dec[b_row[k]];
+    return acc;
+}
+
+/* The same for 8-bit operands. */
+static double dot_row_row8(const double* dec, const uint8_t* a_row, const uint8_t* b_row, int64_t K) {
     double acc = 0.0;
     for (int64_t k = 0; k < K; ++k) acc += dec[a_row[k]] * dec[b_row[k]];
     return acc;
@@ -202,6 +268,14 @@ void oracle_bf16_to_f64(const uint16_t* h, double* out, int64_t n) {
 
 void oracle_f64_to_bf16(const double* x, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = bf16_encode(x[i]);
+}
+
+void oracle_e4m3_to_f64(const uint8_t* h, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_decode(h[i]);
+}
+
+void oracle_e5m2_to_f64(const uint8_t* h, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e5m2_decode(h[i]);
 }
 
 /* ------------------------------------------------------------------ */
@@ -308,17 +382,24 @@ int oracle_gemm_nt_rows(const uint16_t* A, const uint16_t* B, int64_t M, int64_t
 
 /* ------------------------------------------------------------------ */
 /* exported: GEMM with an element type and the fused output transform  */
-/*   D[m,n] = round( act( alpha * S[m,n] + beta * C[m,n] + bias[n] ) )  */
+/*   D[m,n] = round( act( alpha * s[n] * S[m,n] + beta * C[m,n]         */
+/*                        + bias[n] ) )                                 */
 /* with S the plain definition above (fp64, ascending k), every term in */
-/* fp64 and one rounding to the element type at the end.  This is the  */
+/* fp64 and one rounding to the output type at the end.  This is the    */
 /* scaled update C = alpha A B + beta C of the GEMM blog post (section  */
-/* 2.1) with the bias and ReLU fusion it recommends (section 5.4).      */
-/* dtype 0 = fp16, 1 = bf16; C and bias may be NULL; act 0 none, 1 relu. */
+/* 2.1) with the bias and ReLU fusion it recommends (section 5.4).  s[n]*/
+/* is an optional fp32 scale per output column: with 8-bit operands the */
+/* blog post (section 4.2) quantises weights with one scale per output  */
+/* channel (a row of B) and activations with one per tensor (alpha), and*/
+/* passes the scales to the kernel as fp32 numbers.                     */
+/* dtype 0 = fp16 operands and output, 1 = bf16 operands and output,    */
+/* 2 = E4M3 operands, 3 = E5M2 operands (both with bf16 output, C and   */
+/* bias).  C, bias and s may be NULL; act 0 none, 1 relu.               */
 /* ------------------------------------------------------------------ */
 typedef struct {
     int dtype;
-    const uint16_t* A;
-    const uint16_t* B;
+    const void* A;        /* uint16_t bit patterns, or uint8_t for dtype 2 and 3 */
+    const void* B;
     int64_t M, N, K;
     const int64_t* rows;
     const int64_t* cols;
@@ -327,6 +408,7 @@ typedef struct {
     double alpha, beta;
     const uint16_t* C;
     const uint16_t* bias;
+    const float* scale_n;
     int act;
     double* pre;          /* optional: the value before rounding */
     uint16_t* out;
@@ -335,17 +417,26 @@ typedef struct {
     int rows_mode;
 } job_ex_t;
 
-static double element_ex(const job_ex_t* j, const double* dec, int64_t m, int64_t n) {
-    double v = j->alpha * dot_row_row(dec, j->A + m * j->K, j->B + n * j->K, j->K);
-    if (j->C && j->beta != 0.0) v += j->beta * dec[j->C[m * j->N + n]];
-    if (j->bias) v += dec[j->bias[n]];
+static double element_ex(const job_ex_t* j, const double* dec_in, const double* dec_out, int64_t m, int64_t n) {
+    double sum;
+    if (j->dtype >= 2)
+        sum = dot_row_row8(dec_in, (const uint8_t*)j->A + m * j->K, (const uint8_t*)j->B + n * j->K, j->K);
+    else
+        sum = dot_row_row(dec_in, (const uint16_t*)j->A + m * j->K, (const uint16_t*)j->B + n * j->K, j->K);
+    const double scale = j->scale_n ? (double)j->scale_n[n] : 1.0;
+    double v = j->alpha * scale * sum;
+    if (j->C && j->beta != 0.0) v += j->beta * dec_out[j->C[m * j->N + n]];
+    if (j->bias) v += dec_out[j->bias[n]];
     if (j->act == 1 && v < 0.0) v = 0.0;   /* relu: negative values to zero; NaN and -0 pass */
     return v;
 }
 
 static void* ex_worker(void* p) {
     job_ex_t* j = (job_ex_t*)p;
-    const double* dec = j->dtype == 1 ? decode_bf16_table() : decode_table();
+    const double* dec_in = j->dtype == 0 ? decode_table()
+                         : j->dtype == 1 ? decode_bf16_table()
+                         : j->dtype == 2 ? decode_e4m3_table() : decode_e5m2_table();
+    const double* dec_out = j->dtype == 0 ? decode_table() : decode_bf16_table();
     const int64_t total = j->rows_mode ? (j->row_end - j->row_begin) * j->N : j->count;
     const int64_t lo = total * j->tid / j->nthreads;
     const int64_t hi = total * (j->tid + 1) / j->nthreads;
@@ -353,9 +444,9 @@ static void* ex_worker(void* p) {
         int64_t m, n;
         if (j->rows_mode) { m = j->row_begin + i / j->N; n = i % j->N; }
         else { m = j->rows[i]; n = j->cols[i]; }
-        const double v = element_ex(j, dec, m, n);
+        const double v = element_ex(j, dec_in, dec_out, m, n);
         if (j->pre) j->pre[i] = v;
-        j->out[i] = j->dtype == 1 ? bf16_encode(v) : f16_encode(v);
+        j->out[i] = j->dtype == 0 ? f16_encode(v) : bf16_encode(v);
     }
     return NULL;
 }
@@ -385,12 +476,12 @@ static int run_ex(job_ex_t* proto) {
 
 /* Entries (rows[i], cols[i]) when rows != NULL, else rows [row_begin,
  * row_end) written row-major.  Returns 0, or -1 on bad arguments. */
-int oracle_gemm_nt_ex(int dtype, const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+int oracle_gemm_nt_ex(int dtype, const void* A, const void* B, int64_t M, int64_t N, int64_t K,
                       const int64_t* rows, const int64_t* cols, int64_t count,
                       int64_t row_begin, int64_t row_end,
-                      double alpha, double beta, const uint16_t* C, const uint16_t* bias, int act,
-                      double* pre, uint16_t* out, int nthreads) {
-    if ((dtype != 0 && dtype != 1) || M < 0 || N < 0 || K < 0 || (act != 0 && act != 1)) return -1;
+                      double alpha, double beta, const uint16_t* C, const uint16_t* bias,
+                      const float* scale_n, int act, double* pre, uint16_t* out, int nthreads) {
+    if (dtype < 0 || dtype > 3 || M < 0 || N < 0 || K < 0 || (act != 0 && act != 1)) return -1;
     job_ex_t j;
     memset(&j, 0, sizeof j);
     if (rows) {
@@ -403,7 +494,7 @@ int oracle_gemm_nt_ex(int dtype, const uint16_t* A, const uint16_t* B, int64_t M
         j.rows_mode = 1; j.row_begin = row_begin; j.row_end = row_end;
     }
     j.dtype = dtype; j.A = A; j.B = B; j.M = M; j.N = N; j.K = K;
-    j.alpha = alpha; j.beta = beta; j.C = C; j.bias = bias; j.act = act;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.bias = bias; j.scale_n = scale_n; j.act = act;
     j.pre = pre; j.out = out; j.nthreads = nthreads;
     return run_ex(&j);
 }

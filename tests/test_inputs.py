@@ -51,3 +51,27 @@ def test_sample_entries_cover_rows_cols_corners():
     pairs = set(zip(r.tolist(), c.tolist()))
     assert {(0, 0), (0, 59), (99, 0), (99, 59)} <= pairs
     assert all((99, j) in pairs for j in range(60)) and all((i, 59) in pairs for i in range(100))
+
+
+def test_fp8_operands_scaled_to_the_format():
+    torch = __import__("pytest").importorskip("torch")
+    for fmt, tdt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        A, B, sa, sb = inputs.operands_fp8(40, 24, 96, "normal:1/sqrtK", "uniform", seed=7, fmt=fmt)
+        assert A.dtype == np.uint8 and A.shape == (40, 96) and B.shape == (24, 96)
+        assert sb.dtype == np.float32 and sb.shape == (24,)
+        A2, B2, sa2, sb2 = inputs.operands_fp8(40, 24, 96, "normal:1/sqrtK", "uniform", seed=7, fmt=fmt)
+        assert np.array_equal(A, A2) and np.array_equal(B, B2) and sa == sa2 and np.array_equal(sb, sb2)
+        a = torch.from_numpy(A).view(tdt).double().numpy()
+        b = torch.from_numpy(B).view(tdt).double().numpy()
+        top = inputs.FP8_MAX[fmt]
+        assert np.all(np.isfinite(a)) and np.all(np.isfinite(b))
+        assert np.abs(a).max() == top                            # the largest draw maps onto the bound
+        assert np.all(np.abs(b).max(axis=1) == top)              # per row for B
+        # dequantised values follow the fp64 draws to the format's precision
+        x = inputs._draw_f64(40, 96, "normal:1/sqrtK", 7)
+        y = inputs._draw_f64(24, 96, "uniform", 1007)
+        # (half an ulp relative for normals; half the subnormal step absolute)
+        rel, sub = (2.0 ** -4, 2.0 ** -10) if fmt == "e4m3" else (2.0 ** -3, 2.0 ** -17)
+        sbc = sb[:, None].astype(np.float64)
+        assert np.all(np.abs(a * sa - x) <= rel * np.abs(x) + sub * sa * 1.0001)
+        assert np.all(np.abs(b * sbc - y) <= rel * np.abs(y) + sub * sbc * 1.0001)

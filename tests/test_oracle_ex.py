@@ -169,10 +169,10 @@ MUTANTS = {
     "bf16_flushed_subnormals": ("if (expo == 0) v = ldexp((double)frac, -133);", "if (expo == 0) v = 0.0;"),
     "beta_sign": ("if (j->C && j->beta != 0.0) v += j->beta *", "if (j->C && j->beta != 0.0) v -= j->beta *"),
     "alpha_scales_C": ("if (j->C && j->beta != 0.0) v += j->beta *", "if (j->C && j->beta != 0.0) v += j->alpha * j->beta *"),
-    "bias_dropped": ("if (j->bias) v += dec[j->bias[n]];", ";"),
+    "bias_dropped": ("if (j->bias) v += dec_out[j->bias[n]];", ";"),
     "relu_inverted": ("if (j->act == 1 && v < 0.0) v = 0.0;", "if (j->act == 1 && v > 0.0) v = 0.0;"),
-    "ex_double_rounding": ("j->out[i] = j->dtype == 1 ? bf16_encode(v) : f16_encode(v);",
-                           "j->out[i] = j->dtype == 1 ? bf16_encode((double)(float)v) : f16_encode((double)(float)v);"),
+    "ex_double_rounding": ("j->out[i] = j->dtype == 0 ? f16_encode(v) : bf16_encode(v);",
+                           "j->out[i] = j->dtype == 0 ? f16_encode((double)(float)v) : bf16_encode((double)(float)v);"),
 }
 
 
