@@ -36,6 +36,14 @@ sys.path.insert(0, ROOT)
 from dense_fp16_gemm_f16_gb300 import inputs, metrics  # noqa: E402
 
 METRIC = "fp16 GEMM TFLOPS (2MNK/t) at 8192³ on 1 GB300; % of dense-fp16 tensor peak"
+FP8 = ("e4m3", "e5m2")
+
+
+def metric_of(dtype: str) -> str:
+    """The metric line for an operand type (the fp16 one is the headline)."""
+    if dtype in FP8:
+        return f"{dtype} GEMM TFLOPS (2MNK/t), bf16 out, on 1 GB300; % of dense-fp8 tensor peak"
+    return METRIC
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0      # used only if the measured-peaks file is absent
 L2_ROTATE_BYTES = 256 << 20        # about twice the 129 MB L2
@@ -55,8 +63,10 @@ def parse_args():
                     help="time an M x N x K problem (normal(0, 1/sqrt(K)) entries) instead of a named workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
-                    help="operand and output type (bf16 runs the same kernels with bf16 operands)")
+    ap.add_argument("--dtype", choices=["f16", "bf16", "e4m3", "e5m2"], default="f16",
+                    help="operand type: bf16 runs the same kernels with bf16 operands and output; the 8-bit "
+                         "types run the kind::f8f6f4 kernels on amax-scaled operands (one scale for A, one "
+                         "per row of B, applied in the fused epilogue) with a bf16 output")
     ap.add_argument("--epilogue", action="store_true",
                     help="time D = relu(1.5 * A·Bᵀ + 0.5 * C + bias) through gemm_nt_ex instead of the plain product")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,7 +193,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_rows_fn(A, B, dtype="f16", epi=None):
+def oracle_rows_fn(A, B, dtype="f16", epi=None, scales=(None, None)):
     """f(r0, r1, threads): the oracle's rows r0..r1-1 of D for this bench configuration."""
     import oracle
     o = oracle.default()
@@ -191,15 +201,20 @@ def oracle_rows_fn(A, B, dtype="f16", epi=None):
         return lambda r0, r1, threads: o.gemm_rows(A, B, r0, r1, nthreads=threads)
     C, bias = epi if epi is not None else (None, None)
     alpha, beta, relu = (EPI_ALPHA, EPI_BETA, True) if epi is not None else (1.0, 0.0, False)
+    a_scale, b_scale = scales
+    if a_scale is not None:
+        alpha = float(np.float32(alpha * a_scale))     # the fp32 alpha the GPU receives
     return lambda r0, r1, threads: oracle._gemm_ex(o, A, B, dtype, alpha, beta, C, bias, relu,
-                                                   row_begin=r0, row_end=r1, nthreads=threads)
+                                                   row_begin=r0, row_end=r1, nthreads=threads,
+                                                   scale_n=b_scale)
 
 
-def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None, dtype="f16", epi=None):
+def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None, dtype="f16", epi=None,
+                       scales=(None, None)):
     """Time the oracle on a block of output rows sized to take about target_s."""
     import oracle
     threads = oracle.default_threads()
-    fn = oracle_rows_fn(A, B, dtype, epi)
+    fn = oracle_rows_fn(A, B, dtype, epi, scales)
     M, K = A.shape
     t = time.perf_counter()
     fn(0, 1, threads)
@@ -213,10 +228,10 @@ def oracle_rows_timing(A, B, target_s: float, max_rows: int | None = None, dtype
     return rows, dt, threads
 
 
-def cpu_baseline(A, B, target_s: float, dtype="f16", epi=None) -> dict:
+def cpu_baseline(A, B, target_s: float, dtype="f16", epi=None, scales=(None, None)) -> dict:
     M, K = A.shape
     N = B.shape[0]
-    rows, dt, threads = oracle_rows_timing(A, B, target_s, dtype=dtype, epi=epi)
+    rows, dt, threads = oracle_rows_timing(A, B, target_s, dtype=dtype, epi=epi, scales=scales)
     return {"value": metrics.tflops(rows, N, K, dt), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of D ({rows}x{N} outputs, K={K}) of the same seeded "
                       f"operands, fp64 accumulation, {dt:.2f} s"}
@@ -230,9 +245,23 @@ def workload_of(args):
 
 
 def operands_of(w, dtype="f16"):
+    """(A, B, (a_scale, b_scale)); the scales (8-bit operands only) are None otherwise."""
+    if dtype in FP8:
+        if (w.K % 16) != 0:
+            raise SystemExit(f"{w.name}: 8-bit rows of K = {w.K} bytes are not whole 16-byte units")
+        A, B, sa, sb = inputs.operands_fp8(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed, fmt=dtype)
+        return A, B, (sa, sb)
     if dtype == "bf16":
-        return inputs.operands_bf16(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
-    return inputs.operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
+        return (*inputs.operands_bf16(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed), (None, None))
+    return (*inputs.operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed), (None, None))
+
+
+def out_dtype(dtype: str) -> str:
+    return "f16" if dtype == "f16" else "bf16"
+
+
+def in_bytes(dtype: str) -> int:
+    return 1 if dtype in FP8 else 2
 
 
 EPI_ALPHA, EPI_BETA = 1.5, 0.5
@@ -240,7 +269,7 @@ EPI_ALPHA, EPI_BETA = 1.5, 0.5
 
 def epilogue_inputs(w, dtype="f16"):
     """C [M, N] and bias [N] of the fused-epilogue timing, uniform(-1, 1), seeded."""
-    drawf = inputs.draw_bf16 if dtype == "bf16" else inputs.draw
+    drawf = inputs.draw_bf16 if out_dtype(dtype) == "bf16" else inputs.draw
     return drawf(w.M, w.N, "uniform", w.seed + 2000), drawf(1, w.N, "uniform", w.seed + 3000).reshape(w.N)
 
 
@@ -249,10 +278,10 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = workload_of(args)
-    A, B = operands_of(w, args.dtype)
+    A, B, scales = operands_of(w, args.dtype)
     import oracle
     threads = oracle.default_threads()
-    fn = oracle_rows_fn(A, B, args.dtype, epilogue_inputs(w, args.dtype) if args.epilogue else None)
+    fn = oracle_rows_fn(A, B, args.dtype, epilogue_inputs(w, args.dtype) if args.epilogue else None, scales)
     # bound the whole run to a few minutes: size each step's sample of rows
     budget = 120.0
     per_step = max(0.05, min(2.0, budget / max(1, args.steps + args.warmup)))
@@ -272,7 +301,7 @@ def run_reference(args):
     sec = sum(times) / len(times)
     value = metrics.tflops(rows, w.N, w.K, sec)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_of(args.dtype), "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "operands": args.dtype,
@@ -286,7 +315,8 @@ def run_reference(args):
     return 0
 
 
-def run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, A_h, B_h, C_h, bias_h):
+def run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, A_h, B_h, C_h, bias_h,
+            alpha=1.0, scale_h=None):
     """End to end through the C ABI from pinned host memory: every step copies
     its inputs host -> device, runs the GEMM and copies D back.  Steps are
     pipelined the way a caller would run them: inputs of step s+1 travel on a
@@ -301,6 +331,8 @@ def run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, 
     host_in = [pinned(A_h), pinned(B_h)]
     if args.epilogue:
         host_in += [pinned(C_h), pinned(bias_h)]
+    if scale_h is not None:
+        host_in.append(pinned(scale_h))               # the per-column scales are inputs too
     D_pin = [torch.empty((w.M, w.N), dtype=tdt).pin_memory() for _ in range(2)]
     bufs = [[torch.empty_like(h, device=dev) for h in host_in] for _ in range(2)]
     D_dev = [torch.empty((w.M, w.N), dtype=tdt, device=dev) for _ in range(2)]
@@ -310,16 +342,19 @@ def run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, 
     ev_out = [torch.cuda.Event() for _ in range(2)]
     epis = []
     for b in range(2):
+        sc = bufs[b][-1].data_ptr() if scale_h is not None else None
         if args.epilogue:
-            epis.append(g.Epilogue(EPI_ALPHA, EPI_BETA, bufs[b][2].data_ptr(), bufs[b][3].data_ptr(),
-                                   int(g.Activation.RELU), 0))
+            epis.append(g.Epilogue(alpha * EPI_ALPHA, EPI_BETA, bufs[b][2].data_ptr(), bufs[b][3].data_ptr(),
+                                   int(g.Activation.RELU), 0, sc))
+        elif scale_h is not None:
+            epis.append(g.Epilogue(alpha, 0.0, None, None, 0, 0, sc))
         else:
             epis.append(None)
 
     def launch(b):
         a, bb, d = bufs[b][0].data_ptr(), bufs[b][1].data_ptr(), D_dev[b].data_ptr()
         h = stream.cuda_stream
-        if args.epilogue:
+        if epis[b] is not None:
             st = lib.gemm_nt_ex(dtype_code, a, bb, d, w.M, w.N, w.K, g.ctypes.byref(epis[b]), 0, h)
         elif args.dtype == "bf16":
             st = lib.gemm_bf16_nt(a, bb, d, w.M, w.N, w.K, h)
@@ -364,8 +399,8 @@ def run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, 
     e2e_ms = max_over_ranks(pg, e2e_ms, dev)
     g.gemm_f16_nt_check(stream=stream, device=dev)
     return {"value": job_tflops(world, w.M, w.N, w.K, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-            "h2d_bytes_per_step": sum(h.numel() * 2 for h in host_in),
-            "d2h_bytes_per_step": D_pin[0].numel() * 2,
+            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_in),
+            "d2h_bytes_per_step": D_pin[0].numel() * D_pin[0].element_size(),
             "pipelining": "inputs of the next step and D of the previous one move on their own "
                           "streams while a step computes (two buffer sets)"}
 
@@ -394,24 +429,28 @@ def run_ours(args):
         pg.barrier()
     g.load()
     w = workload_of(args)
-    A_h, B_h = operands_of(w, args.dtype)
-    tdt = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    A_h, B_h, (a_scale, b_scale_h) = operands_of(w, args.dtype)
+    tdt = torch.bfloat16 if out_dtype(args.dtype) == "bf16" else torch.float16
+    dtype_code = int({"f16": g.Dtype.F16, "bf16": g.Dtype.BF16, "e4m3": g.Dtype.E4M3,
+                      "e5m2": g.Dtype.E5M2}[args.dtype])
 
     def to_torch(x):
-        # bf16 operands travel as uint16 bit patterns
-        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if args.dtype == "bf16" else x)
-        return t.view(tdt)
+        # bf16 values travel as uint16 bit patterns, 8-bit operands as uint8
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(x)
 
     stream = torch.cuda.Stream(device=dev)
     A = to_torch(A_h).to(dev)
     B = to_torch(B_h).to(dev)
     D = torch.empty((w.M, w.N), dtype=tdt, device=dev)
-    plan = g.gemm_f16_nt_plan(w.M, w.N, w.K)
+    plan = g.gemm_nt_plan_ex(dtype_code, w.M, w.N, w.K)
     lib = g.load()
     s_handle = stream.cuda_stream
     # Operands smaller than twice the L2 are rotated over enough copies that
     # consecutive launches never find them in L2 (no flush needed between them).
-    ab_bytes = (w.M * w.K + w.N * w.K) * 2
+    ab_bytes = (w.M * w.K + w.N * w.K) * in_bytes(args.dtype)
     copies = 1 if ab_bytes >= L2_ROTATE_BYTES else max(4, min(64, -(-L2_ROTATE_BYTES // max(ab_bytes, 1))))
     As, Bs = [A], [B]
     for _ in range(copies - 1):
@@ -422,14 +461,21 @@ def run_ours(args):
     d_ptr = D.data_ptr()
     cur = [0]
     C_h = bias_h = C = bias = None
+    # 8-bit operands: the per-tensor scale of A is alpha, B's per-row scales scale D's columns
+    alpha = float(np.float32(a_scale)) if a_scale is not None else 1.0
+    scale_n = torch.from_numpy(b_scale_h).to(dev) if b_scale_h is not None else None
+    sc_ptr = scale_n.data_ptr() if scale_n is not None else None
     if args.epilogue:
         C_h, bias_h = epilogue_inputs(w, args.dtype)
         C, bias = to_torch(C_h).to(dev), to_torch(bias_h).to(dev)
-        epi = g.Epilogue(EPI_ALPHA, EPI_BETA, C.data_ptr(), bias.data_ptr(), int(g.Activation.RELU), 0)
+        epi = g.Epilogue(alpha * EPI_ALPHA, EPI_BETA, C.data_ptr(), bias.data_ptr(), int(g.Activation.RELU), 0,
+                         sc_ptr)
         epi_ref = g.ctypes.byref(epi)
-    dtype_code = int(g.Dtype.BF16 if args.dtype == "bf16" else g.Dtype.F16)
+    elif scale_n is not None:
+        epi = g.Epilogue(alpha, 0.0, None, None, 0, 0, sc_ptr)
+        epi_ref = g.ctypes.byref(epi)
 
-    if args.epilogue:
+    if args.epilogue or scale_n is not None:
         def step():
             i = cur[0] = (cur[0] + 1) % copies
             st = lib.gemm_nt_ex(dtype_code, a_ptrs[i], b_ptrs[i], d_ptr, w.M, w.N, w.K, epi_ref, 0, s_handle)
@@ -502,7 +548,8 @@ def run_ours(args):
     # end to end through the C ABI: pinned host operands in, pinned host result out
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, A_h, B_h, C_h, bias_h)
+        e2e = run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, A_h, B_h, C_h, bias_h,
+                      alpha, b_scale_h)
 
     clocks = sampler.stop() if sampler else None
     if pg:
@@ -512,20 +559,25 @@ def run_ours(args):
         return 0
 
     peaks = measured_peaks()
+    # dense fp16 and bf16 tensor rates are the same on this architecture (ratio 1);
+    # the dense fp8 rate is twice that (nominal 4.5 against 2.25 PFLOP/s)
+    ratio = 2.0 if args.dtype in FP8 else 1.0
     if peaks and peaks.get("bf16_tflops"):
-        # dense fp16 and bf16 tensor rates are the same on this architecture (ratio 1)
-        peak = float(peaks["bf16_tflops"])
-        peak_src = "measured (bf16 cuBLAS burst, fp16 rate = bf16 rate)"
+        peak = float(peaks["bf16_tflops"]) * ratio
+        peak_src = ("measured bf16 cuBLAS burst x 2 (nominal dense fp8 : bf16 ratio)" if ratio != 1.0 else
+                    "measured (bf16 cuBLAS burst, fp16 rate = bf16 rate)")
     else:
-        peak = FALLBACK_PEAK_TFLOPS
-        peak_src = "fallback"
+        peak = FALLBACK_PEAK_TFLOPS * ratio
+        peak_src = "fallback" + (" x 2 (nominal dense fp8 : bf16 ratio)" if ratio != 1.0 else "")
     achieved = metrics.tflops(w.M, w.N, w.K, launch_ms * 1e-3)
     # the ncu counters were taken on the plain fp16 product
     traffic = recorded_traffic(w.name) if args.dtype == "f16" and not args.epilogue else None
     if plan["variant"] == "SKINNY_SPLITK":
         hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else 6800.0
-        # algorithmic bytes: A and B read once, D written once (+ C and bias read with the epilogue)
-        alg_bytes = w.compulsory_bytes + (w.M * w.N * 2 + w.N * 2 if args.epilogue else 0)
+        # algorithmic bytes: A and B read once, D written once (+ C and bias read with the
+        # epilogue, + the per-column scales of 8-bit operands)
+        alg_bytes = ((w.M * w.K + w.N * w.K) * in_bytes(args.dtype) + w.M * w.N * 2
+                     + (w.M * w.N * 2 + w.N * 2 if args.epilogue else 0) + (w.N * 4 if b_scale_h is not None else 0))
         gbs = metrics.gbs(alg_bytes, launch_ms * 1e-3)
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                     "traffic": traffic, "peak_source": "measured" if peaks else "fallback"}
@@ -535,13 +587,17 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(A_h, B_h, args.cpu_seconds, args.dtype, (C_h, bias_h) if args.epilogue else None)
+        cpu = cpu_baseline(A_h, B_h, args.cpu_seconds, args.dtype, (C_h, bias_h) if args.epilogue else None,
+                           (a_scale, b_scale_h))
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_of(args.dtype), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "accumulate": "f32",
+                   "output": out_dtype(args.dtype),
+                   "scales": ("A per tensor (alpha), B per row (per-column scale of D), fp32" if b_scale_h is not None
+                              else "none"),
                    "epilogue": (f"relu({EPI_ALPHA} * A·Bᵀ + {EPI_BETA} * C + bias)" if args.epilogue else "none"),
                    "variant": plan["variant"], "grid_ctas": plan["grid_ctas"],
                    "l2": (f"inputs larger than L2 (A+B = {ab_bytes >> 20} MiB >= {L2_ROTATE_BYTES >> 20} MiB); no flush"

@@ -47,6 +47,8 @@ class Variant(enum.IntEnum):
 class Dtype(enum.IntEnum):
     F16 = 0
     BF16 = 1
+    E4M3 = 2   # 8-bit operands, bf16 D
+    E5M2 = 3
 
 
 class Activation(enum.IntEnum):
@@ -55,9 +57,10 @@ class Activation(enum.IntEnum):
 
 
 class Epilogue(ctypes.Structure):
-    """Mirror of gemm_epilogue_t: D = act(alpha * (A Bᵀ) + beta * C + bias[n])."""
+    """Mirror of gemm_epilogue_t: D = act(alpha * scale_n[n] * (A Bᵀ) + beta * C + bias[n])."""
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("C", ctypes.c_void_p),
-                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("scale_n", ctypes.c_void_p)]
 
 
 class LibraryMissing(RuntimeError):
@@ -115,6 +118,9 @@ def load():
         lib.gemm_bf16_nt.restype = ctypes.c_int
         lib.gemm_nt_ex.argtypes = [ctypes.c_int, p, p, p, i64, i64, i64, ctypes.POINTER(Epilogue), ctypes.c_int, p]
         lib.gemm_nt_ex.restype = ctypes.c_int
+        lib.gemm_nt_plan_ex.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_int, ctypes.c_int32,
+                                        ctypes.POINTER(Plan)]
+        lib.gemm_nt_plan_ex.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -139,16 +145,28 @@ def _stream_handle(stream, device=None) -> int | None:
     return int(stream) or None
 
 
+def _torch_types(dtype):
+    """(accepted operand dtypes, D dtype) for a Dtype."""
+    import torch
+    if dtype == Dtype.BF16:
+        return (torch.bfloat16,), torch.bfloat16
+    if dtype == Dtype.E4M3:
+        return (torch.float8_e4m3fn, torch.uint8), torch.bfloat16
+    if dtype == Dtype.E5M2:
+        return (torch.float8_e5m2, torch.uint8), torch.bfloat16
+    return (torch.float16,), torch.float16
+
+
 def _operands(A, B, D, M, N, K, dtype=None):
     """(a_ptr, b_ptr, d_ptr, M, N, K, device) from tensors or raw pointers."""
     if _is_tensor(A):
-        import torch
-        want = torch.bfloat16 if dtype == Dtype.BF16 else torch.float16
+        ins, out = _torch_types(Dtype.F16 if dtype is None else dtype)
         for name, t in (("A", A), ("B", B), ("D", D)):
             if not _is_tensor(t):
                 raise TypeError(f"{name}: mix of tensors and raw pointers")
-            if t.dtype != want:
-                raise TypeError(f"{name} must be {want}, got {t.dtype}")
+            want = (out,) if name == "D" else ins
+            if t.dtype not in want:
+                raise TypeError(f"{name} must be {' or '.join(map(str, want))}, got {t.dtype}")
             if not t.is_cuda:
                 raise ValueError(f"{name} must be a CUDA tensor")
             if t.dim() != 2 or not t.is_contiguous():
@@ -216,24 +234,35 @@ def gemm_bf16_nt(A, B, D, M=None, N=None, K=None, stream=None) -> None:
 
 def _tensor_dtype(A):
     import torch
-    return Dtype.BF16 if getattr(A, "dtype", None) == torch.bfloat16 else Dtype.F16
+    return {torch.bfloat16: Dtype.BF16, torch.float8_e4m3fn: Dtype.E4M3,
+            torch.float8_e5m2: Dtype.E5M2}.get(getattr(A, "dtype", None), Dtype.F16)
 
 
 def gemm_nt_ex(A, B, D, M=None, N=None, K=None, dtype=None, alpha=1.0, beta=0.0, C=None, bias=None,
-               activation=Activation.NONE, variant=Variant.AUTO, stream=None) -> None:
-    """D = act(alpha·A·Bᵀ + beta·C + bias[n]) for fp16 or bf16 (dtype taken from the tensors)."""
+               activation=Activation.NONE, variant=Variant.AUTO, stream=None, scale_n=None) -> None:
+    """D = act(alpha·scale_n[n]·A·Bᵀ + beta·C + bias[n]).
+
+    Operands fp16, bf16, or 8-bit (E4M3 / E5M2, as torch float8 or uint8
+    tensors; D, C and bias are then bf16); the dtype is taken from the tensors
+    unless given (uint8 tensors need it).  ``scale_n`` is an optional float32
+    [N] tensor (or device pointer) of per-column scales."""
     if dtype is None:
         dtype = _tensor_dtype(A) if _is_tensor(A) else Dtype.F16
     a, b, d, m, n, k, dev = _operands(A, B, D, M, N, K, Dtype(dtype))
-    def ptr(x):
+    def ptr(x, what="C and bias", want=None):
         if x is None:
             return None
         if _is_tensor(x):
-            if x.dtype != D.dtype or not x.is_contiguous():
-                raise TypeError("C and bias must be contiguous and of D's dtype")
+            want = D.dtype if want is None else want
+            if x.dtype != want or not x.is_contiguous():
+                raise TypeError(f"{what} must be contiguous {want}")
             return x.data_ptr()
         return int(x)
-    epi = Epilogue(float(alpha), float(beta), ptr(C), ptr(bias), int(activation), 0)
+    sc = None
+    if scale_n is not None:
+        import torch
+        sc = ptr(scale_n, "scale_n", torch.float32)
+    epi = Epilogue(float(alpha), float(beta), ptr(C), ptr(bias), int(activation), 0, sc)
     _call("gemm_nt_ex", (int(dtype), a or None, b or None, d or None, m, n, k, ctypes.byref(epi), int(variant),
                          _stream_handle(stream, dev)), dev)
 
@@ -250,6 +279,15 @@ def gemm_f16_nt_plan(M: int, N: int, K: int, variant=Variant.AUTO, num_sms: int 
     st = load().gemm_f16_nt_plan(int(M), int(N), int(K), int(variant), int(num_sms), ctypes.byref(plan))
     if st != Status.OK:
         raise GemmError(st, "gemm_f16_nt_plan")
+    return plan.as_dict()
+
+
+def gemm_nt_plan_ex(dtype, M: int, N: int, K: int, variant=Variant.AUTO, num_sms: int = 0) -> dict:
+    """gemm_f16_nt_plan for the operand type ``dtype`` (a ``Dtype``)."""
+    plan = Plan()
+    st = load().gemm_nt_plan_ex(int(dtype), int(M), int(N), int(K), int(variant), int(num_sms), ctypes.byref(plan))
+    if st != Status.OK:
+        raise GemmError(st, "gemm_nt_plan_ex")
     return plan.as_dict()
 
 

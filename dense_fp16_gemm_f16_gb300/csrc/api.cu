@@ -65,11 +65,11 @@ constexpr int64_t kL2GroupBytes = 48ll << 20;
 // AUTO uses split-K for the pair kernel only from this many K blocks up.
 constexpr int64_t kSplitKMinBlocks = 40;
 
-int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K) {
+int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K, int in_bytes) {
 #ifdef GEMM_GROUP_M
     const int64_t g = GEMM_GROUP_M;
 #else
-    const int64_t g_max = kL2GroupBytes / (static_cast<int64_t>(tile_m) * K * 2);
+    const int64_t g_max = kL2GroupBytes / (static_cast<int64_t>(tile_m) * K * in_bytes);
     const int64_t groups = g_max < 1 ? m_tiles : cdiv(m_tiles, g_max);
     const int64_t g = cdiv(m_tiles, groups);
 #endif
@@ -78,12 +78,23 @@ int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K) {
 
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
-gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K) {
+// in_bytes: bytes per element of A and B (2, or 1 for 8-bit operands).  Rows
+// of A, B and D must be whole 16-byte units (TMA row pitches).
+gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, int in_bytes = 2) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0 || K == 0) return GEMM_OK;
-    if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_MISALIGNED;
+    if ((K * in_bytes) % 16 != 0 || N % 8 != 0) return GEMM_ERR_MISALIGNED;
     return GEMM_OK;
+}
+
+int dtype_in_bytes(int dtype) { return dtype >= GEMM_DTYPE_E4M3 ? 1 : 2; }
+bool dtype_valid(int dtype) { return dtype >= GEMM_DTYPE_F16 && dtype <= GEMM_DTYPE_E5M2; }
+// element type of D, C and bias: fp16 for fp16 operands, bf16 otherwise
+int dtype_out(int dtype) { return dtype == GEMM_DTYPE_F16 ? GEMM_DTYPE_F16 : GEMM_DTYPE_BF16; }
+// operand format field of the MMA instruction descriptor
+uint32_t dtype_ab_format(int dtype) {
+    return (dtype == GEMM_DTYPE_BF16 || dtype == GEMM_DTYPE_E5M2) ? 1u : 0u;
 }
 
 // ----------------------------------------------------------------- planner
@@ -108,10 +119,11 @@ const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant, const Limits& lim,
-                        gemm_plan_t* pl) {
+                        gemm_plan_t* pl, int in_bytes = 2) {
     std::memset(pl, 0, sizeof(*pl));
-    const gemm_status_t st = check_sizes(M, N, K);
+    const gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
+    const int64_t bk = stage_k(in_bytes);
     if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
@@ -134,23 +146,25 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // (measured on GB300: 512x2048x8192 22.9 us split vs 39.1 us on
             // 128x256 tiles; 1024x1024x2048 15.8 us split vs 12.7 us).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
-            // When K is not a multiple of 16 the rows of A and B do not start on
-            // 32-byte sectors, so every 128-byte TMA row reads five sectors
+            // When a row of A and B (K elements) is not a whole number of 32-byte
+            // sectors, the rows do not start on sectors and every 128-byte TMA row
+            // reads five sectors
             // instead of four; then the 4-CTA clusters, which fetch each B block
             // once for two pairs, win despite using 144 of the 152 SMs (measured
             // on GB300: 4000x11000x4104 226 us against 253 us on pairs, K = 4136
             // 220 against 252; with sector-aligned rows pairs are faster or
             // level: 8192^3 641 against 656 us, K = 4112 207 against 212).
-            if (t2 >= pairs) variant = (K % 16 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
-            else if (cdiv(K, kBK) >= kSplitKMinBlocks && choose_ksplit(t2, pairs, cdiv(K, kBK)) > 1)
+            if (t2 >= pairs)
+                variant = ((K * in_bytes) % 32 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
+            else if (cdiv(K, bk) >= kSplitKMinBlocks && choose_ksplit(t2, pairs, cdiv(K, bk)) > 1)
                 variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
             else if (cdiv(M, 128) * cdiv(N, 256) >= 2) variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else variant = GEMM_VARIANT_TILE_1CTA_128x128;
         }
     }
     pl->variant = variant;
-    pl->tile_k = kBK;
-    pl->k_blocks = cdiv(K, kBK);
+    pl->tile_k = static_cast<int32_t>(bk);
+    pl->k_blocks = cdiv(K, bk);
 
     if (variant == GEMM_VARIANT_SKINNY_SPLITK) {
         const int mn = skinny_mn(M);
@@ -222,7 +236,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     pl->grid_ctas = static_cast<int32_t>(clusters * ops.cluster);
     pl->num_full_tiles = num_full;
     pl->tail_split = split;
-    pl->group_m = static_cast<int32_t>(raster_group(pl->m_tiles, ops.tile_m, K));
+    pl->group_m = static_cast<int32_t>(raster_group(pl->m_tiles, ops.tile_m, K, in_bytes));
     return GEMM_OK;
 }
 
@@ -265,7 +279,7 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
             return GEMM_ERR_CUDA;
         }
         const TiledOps* tiled[3] = {&tiled_ops_2cta256(0), &tiled_ops_1cta128(0), &tiled_ops_1cta256(0)};
-        for (int dt : {0, 1}) {
+        for (int dt : {0, 1, 2}) {   // fp16, bf16, 8-bit (one kernel for both formats)
             const TiledOps* all[4] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt),
                                       &tiled_ops_4cta512(dt)};
             for (const TiledOps* t : all)
@@ -297,15 +311,19 @@ Limits limits_of(const DeviceState& d) {
     return Limits{d.sms, d.max_clusters_2cta, d.max_clusters_4cta, d.per_sm_1cta128, d.per_sm_1cta256};
 }
 
-// 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
-// box of box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
+// 2-D tensor map of a gemm_dtype_t's elements (fp16, bf16, or bytes for the
+// 8-bit types): `inner` contiguous elements per row, `outer` rows, box of
+// box_inner x box_outer elements, 128-byte swizzle, zero fill outside.
 bool encode_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, uint32_t box_inner,
                uint32_t box_outer, int dtype = 0) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * dtype_in_bytes(dtype)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = g_encode(map, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+    const CUtensorMapDataType type = dtype >= GEMM_DTYPE_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims,
                                 strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -385,6 +403,7 @@ EpiParams epi_params(const gemm_epilogue_t* e) {
     p.beta = 0.0f;
     p.C = nullptr;
     p.bias = nullptr;
+    p.scale_n = nullptr;
     p.act = 0;
     p.on = 0;
     if (e == nullptr) return p;
@@ -392,8 +411,9 @@ EpiParams epi_params(const gemm_epilogue_t* e) {
     p.beta = e->beta;
     p.C = e->beta != 0.0f ? e->C : nullptr;
     p.bias = e->bias;
+    p.scale_n = e->scale_n;
     p.act = e->activation;
-    p.on = (p.alpha != 1.0f || p.C != nullptr || p.bias != nullptr || p.act != 0) ? 1 : 0;
+    p.on = (p.alpha != 1.0f || p.C != nullptr || p.bias != nullptr || p.scale_n != nullptr || p.act != 0) ? 1 : 0;
     return p;
 }
 
@@ -401,20 +421,24 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
                   gemm_variant_t variant, gemm_stream_t stream, int dtype = 0,
                   const gemm_epilogue_t* epilogue = nullptr) {
     // ---- host-only argument checks (nothing touches a device before these pass)
-    gemm_status_t st = check_sizes(M, N, K);
+    if (!dtype_valid(dtype)) return GEMM_ERR_INVALID_VALUE;
+    const int in_bytes = dtype_in_bytes(dtype);
+    gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
-    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_VALUE;
     const EpiParams epi = epi_params(epilogue);
     if (epilogue != nullptr) {
         if (epilogue->activation != GEMM_ACT_NONE && epilogue->activation != GEMM_ACT_RELU)
             return GEMM_ERR_INVALID_VALUE;
         if (epilogue->beta != 0.0f && epilogue->C == nullptr) return GEMM_ERR_INVALID_VALUE;
-        if ((epi.C && !aligned16(epi.C)) || (epi.bias && !aligned16(epi.bias))) return GEMM_ERR_MISALIGNED;
+        if ((epi.C && !aligned16(epi.C)) || (epi.bias && !aligned16(epi.bias)) ||
+            (epi.scale_n && !aligned16(epi.scale_n)))
+            return GEMM_ERR_MISALIGNED;
         // C may be D itself (an in-place update); it may not partly overlap D, and
-        // the bias may not overlap D at all
+        // neither the bias nor the scales may overlap D at all
         if (M > 0 && N > 0) {
             if (epi.C && epi.C != D && ranges_overlap(epi.C, M * N * 2, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
             if (epi.bias && ranges_overlap(epi.bias, N * 2, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
+            if (epi.scale_n && ranges_overlap(epi.scale_n, N * 4, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
     if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
@@ -422,7 +446,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     if (M == 0 || N == 0) return GEMM_OK;
     if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
     if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
-    const int64_t a_bytes = M * K * 2, b_bytes = N * K * 2, d_bytes = M * N * 2;
+    const int64_t a_bytes = M * K * in_bytes, b_bytes = N * K * in_bytes, d_bytes = M * N * 2;
     if (ranges_overlap(D, d_bytes, A, a_bytes) || ranges_overlap(D, d_bytes, B, b_bytes))
         return GEMM_ERR_INVALID_VALUE;
     if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_MISALIGNED;
@@ -432,11 +456,13 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     st = get_device(&dev, &dev_id);
     if (st != GEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int out_dtype = dtype_out(dtype);
+    const int bk = stage_k(in_bytes);
 
     if (K == 0) {  // the empty sum
         if (epi.on) {
             const int blocks = static_cast<int>(std::min<int64_t>(cdiv(M * N, 256), 8 * dev->sms));
-            if (dtype == GEMM_DTYPE_BF16)
+            if (out_dtype == GEMM_DTYPE_BF16)
                 epilogue_only_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(D), M, N, epi);
             else
                 epilogue_only_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<__half*>(D), M, N, epi);
@@ -451,14 +477,14 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     }
 
     gemm_plan_t pl;
-    st = make_plan(M, N, K, variant, limits_of(*dev), &pl);
+    st = make_plan(M, N, K, variant, limits_of(*dev), &pl, in_bytes);
     if (st != GEMM_OK) return st;
 
     if (pl.variant == GEMM_VARIANT_SKINNY_SPLITK) {
         const SkinnyOps& ops = skinny_ops(pl.tile_m, dtype);
         CUtensorMap tw, tx;
-        if (!encode_2d(&tw, B, K, N, kBK, 128, dtype) ||
-            !encode_2d(&tx, A, K, M, kBK, static_cast<uint32_t>(ops.mn), dtype))
+        if (!encode_2d(&tw, B, K, N, bk, 128, dtype) ||
+            !encode_2d(&tx, A, K, M, bk, static_cast<uint32_t>(ops.mn), dtype))
             return GEMM_ERR_INVALID_VALUE;
         Workspace* ws = nullptr;
         const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
@@ -479,7 +505,8 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         p.epi = epi;
         p.status = dev->status;
         p.timeout_ns = timeout_for(pl.k_blocks);
-        p.stream_b = N * K * 2 >= kStreamBBytes ? 1 : 0;
+        p.stream_b = b_bytes >= kStreamBBytes ? 1 : 0;
+        p.ab_format = dtype_ab_format(dtype);
         if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
@@ -497,9 +524,9 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     }
     CUtensorMap ta, tb, tbp, td;
     const uint32_t b_rows = static_cast<uint32_t>(ops.b_box_rows);
-    if (!encode_2d(&ta, A, K, M, kBK, 128, dtype) || !encode_2d(&tb, B, K, N, kBK, b_rows, dtype) ||
-        !encode_2d(&tbp, B, K, N, kBK, b_rows / static_cast<uint32_t>(pl.tail_split), dtype) ||
-        !encode_2d(&td, D, N, M, 64, 32, dtype))
+    if (!encode_2d(&ta, A, K, M, bk, 128, dtype) || !encode_2d(&tb, B, K, N, bk, b_rows, dtype) ||
+        !encode_2d(&tbp, B, K, N, bk, b_rows / static_cast<uint32_t>(pl.tail_split), dtype) ||
+        !encode_2d(&td, D, N, M, 64, 32, out_dtype))
         return GEMM_ERR_INVALID_VALUE;
     TiledParams p;
     p.M = static_cast<int32_t>(M);
@@ -513,6 +540,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.num_full = pl.num_full_tiles;
     p.split = pl.tail_split;
     p.ksplit = pl.k_split;
+    p.ab_format = dtype_ab_format(dtype);
     p.num_units = pl.k_split > 1 ? p.num_tiles * pl.k_split
                                  : pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
     p.partials = ws ? ws->partials : nullptr;
@@ -619,6 +647,7 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
     p.status = dev->status;
     p.timeout_ns = timeout_for(pl.k_blocks);
     p.stream_b = N * K * 2 >= kStreamBBytes ? 1 : 0;
+    p.ab_format = dtype_ab_format(GEMM_DTYPE_F16);
     if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -686,7 +715,9 @@ GEMM_API const char* gemm_status_string(gemm_status_t status) {
     switch (status) {
         case GEMM_OK: return "GEMM_OK";
         case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: bad size, pointer, overlap or variant";
-        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: pointers must be 16-byte aligned, K and N multiples of 8";
+        case GEMM_ERR_MISALIGNED:
+            return "GEMM_ERR_MISALIGNED: pointers must be 16-byte aligned, N a multiple of 8 and K of 8 "
+                   "(16 for 8-bit operands)";
         case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel gave up waiting on a barrier";
@@ -708,6 +739,21 @@ GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_va
         lim = limits_of(*dev);
     }
     return make_plan(M, N, K, variant, lim, plan);
+}
+
+GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
+                                       int32_t num_sms, gemm_plan_t* plan) {
+    if (plan == nullptr || !dtype_valid(dtype)) return GEMM_ERR_INVALID_VALUE;
+    Limits lim;
+    if (num_sms > 0) {
+        lim = Limits{num_sms, num_sms / 2, num_sms / 4, 1, 1};
+    } else {
+        DeviceState* dev = nullptr;
+        const gemm_status_t st = get_device(&dev, nullptr);
+        if (st != GEMM_OK) return st;
+        lim = limits_of(*dev);
+    }
+    return make_plan(M, N, K, variant, lim, plan, dtype_in_bytes(dtype));
 }
 
 GEMM_API gemm_status_t gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N,

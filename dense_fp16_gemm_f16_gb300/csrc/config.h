@@ -16,10 +16,15 @@
 
 namespace gemm_gb300 {
 
-// One pipeline stage covers 64 K elements: one 128-byte row of fp16, the
+// One pipeline stage moves one 128-byte row of A and of B per tile row: the
 // width of the 128-byte swizzle ("Building a Tiled GEMM", step 1: BLK_K = 64
-// with a 128-byte-swizzled SMEM layout).
-constexpr int kBK = 64;
+// fp16 with a 128-byte-swizzled SMEM layout).  That is 64 K elements of fp16
+// or bf16 and 128 of an 8-bit type.  One MMA instruction takes 32 bytes of
+// each row (K = 16 for 16-bit types, 32 for 8-bit ones): four per stage.
+constexpr int kStageRowBytes = 128;
+constexpr int kMmaPerStage = kStageRowBytes / 32;
+GEMM_HD constexpr int stage_k(int elem_bytes) { return kStageRowBytes / elem_bytes; }
+constexpr int kBK = stage_k(2);   // K elements per stage for 16-bit operands
 // Warp roles of every kernel: warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues the MMAs, warps 2..5 are the epilogue warpgroup (warp w reads TMEM
 // lanes 32*(w%4) .. 32*(w%4)+31).
@@ -62,8 +67,8 @@ struct TiledConfig {
     static constexpr int UNIT_M = BM * PAIRS;                 // rows of a cluster tile
     static constexpr int A_ROWS = 128;
     static constexpr int B_ROWS = BN / CG;
-    static constexpr int A_BYTES = A_ROWS * kBK * 2;
-    static constexpr int B_BYTES = B_ROWS * kBK * 2;
+    static constexpr int A_BYTES = A_ROWS * kStageRowBytes;
+    static constexpr int B_BYTES = B_ROWS * kStageRowBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
     static constexpr int TMEM_COLS = 2 * BN;                 // two accumulator buffers
     static constexpr int EPI_COLS = 64;                      // columns per TMA store box
@@ -105,6 +110,7 @@ struct TiledParams {
     int64_t num_units;        // num_full + (num_tiles - num_full) * split
     int32_t split;            // the remaining tiles are cut into `split` column pieces
     int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces (split-K)
+    uint32_t ab_format;       // operand format field of the MMA instruction descriptor
     float* partials;          // split-K: [num_tiles][ksplit][BM][BN] fp32
     uint32_t* counters;       // split-K: [num_tiles], zero between calls
     void* D;                  // the output (fp16 or bf16 [M][N]); written directly by the
@@ -213,8 +219,8 @@ inline int choose_ksplit(int64_t tiles, int64_t slots, int64_t k_blocks) {
 template <int MN_>
 struct SkinnyConfig {
     static constexpr int MN = MN_;
-    static constexpr int W_BYTES = 128 * kBK * 2;   // weight (B) tile: 128 rows
-    static constexpr int X_BYTES = MN * kBK * 2;    // activation (A) tile: MN rows
+    static constexpr int W_BYTES = 128 * kStageRowBytes;   // weight (B) tile: 128 rows
+    static constexpr int X_BYTES = MN * kStageRowBytes;    // activation (A) tile: MN rows
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
     // This kernel streams B once and is bound by how many bytes are in flight,
     // so the ring takes every stage that fits beside the barriers (12 / 11 / 9).
@@ -249,6 +255,7 @@ struct SkinnyParams {
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t stream_b;         // B is too large to stay in L2: load it evict-first
+    uint32_t ab_format;       // operand format field of the MMA instruction descriptor
 };
 
 // B of at least this many bytes is read once per call and cannot stay in the

@@ -1,15 +1,19 @@
 // epilogue.cuh -- element types and the fused output transform.
 //
-// The kernels run for fp16 or bf16 operands (same tcgen05 kind::f16 MMA with
-// an fp32 accumulator; only the operand format bits of the instruction
-// descriptor differ) and write D in the operand type, rounded to nearest even.
+// The kernels run for fp16 or bf16 operands (tcgen05 kind::f16) and for
+// E4M3 or E5M2 operands (kind::f8f6f4), always with an fp32 accumulator; the
+// operand format is a field of the instruction descriptor.  D is written in
+// the operand type for 16-bit operands and in bf16 for 8-bit ones, rounded to
+// nearest even.
 //
 // The optional fused epilogue computes, in fp32 and before that single
-// rounding,   D = act(alpha * (A B^T) + beta * C + bias[n])
+// rounding,   D = act(alpha * s[n] * (A B^T) + beta * C + bias[n])
 // -- the scaled update C = alpha A B + beta C of the GEMM blog post (section
 // 2.1) with the bias and activation fusion it recommends (section 5.4), and
 // the "epilogue fusion" the Croqtile tutorial credits cuBLAS with in its
-// comparison section.
+// comparison section.  s[n] is an optional fp32 scale per output column: the
+// per-channel weight scale of the blog post's 8-bit quantisation (section
+// 4.2), with the per-tensor activation scale folded into alpha.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -24,6 +28,7 @@ struct EpiParams {
     float beta;
     const void* C;      // [M][N] like D, or nullptr
     const void* bias;   // [N], or nullptr
+    const float* scale_n;  // [N] fp32, or nullptr
     int32_t act;        // 0 none, 1 relu
     int32_t on;         // 0: plain D = A B^T (the other fields are ignored)
 };
@@ -33,7 +38,6 @@ struct Elem;
 
 template <>
 struct Elem<__half> {
-    static constexpr uint32_t kFormat = 0;   // instruction-descriptor A/B format: f16
     __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
         const __half2 x = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&x);
@@ -50,7 +54,6 @@ struct Elem<__half> {
 
 template <>
 struct Elem<__nv_bfloat16> {
-    static constexpr uint32_t kFormat = 1;   // instruction-descriptor A/B format: bf16
     __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
         const __nv_bfloat162 x = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&x);
@@ -76,8 +79,16 @@ __device__ __forceinline__ uint4 epi_load_c8(const EpiParams& e, int64_t row, in
 // output row, given that row's C values from epi_load_c8.
 template <class T>
 __device__ __forceinline__ void epi_apply8_c(const EpiParams& e, float (&x)[8], uint4 c, int64_t col) {
+    if (e.scale_n != nullptr) {
+        const float4 s0 = *reinterpret_cast<const float4*>(e.scale_n + col);
+        const float4 s1 = *reinterpret_cast<const float4*>(e.scale_n + col + 4);
+        const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] *= e.alpha;
+        for (int i = 0; i < 8; ++i) x[i] *= e.alpha * s[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= e.alpha;
+    }
     if (e.C != nullptr && e.beta != 0.0f) {
         const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -105,7 +116,7 @@ __device__ __forceinline__ void epi_apply8_c(const EpiParams& e, float (&x)[8], 
 // element at a time).
 template <class T>
 __device__ __forceinline__ float epi_apply1(const EpiParams& e, float x, int64_t row, int64_t col, int64_t N) {
-    x *= e.alpha;
+    x *= e.scale_n != nullptr ? e.alpha * e.scale_n[col] : e.alpha;
     if (e.C != nullptr && e.beta != 0.0f) x += e.beta * Elem<T>::to_float(static_cast<const T*>(e.C)[row * N + col]);
     if (e.bias != nullptr) x += Elem<T>::to_float(static_cast<const T*>(e.bias)[col]);
     if (e.act == 1) x = x < 0.0f ? 0.0f : x;
@@ -121,6 +132,7 @@ template <class T, int MN>
 struct EpiColumn {
     uint32_t c[(MN + 1) / 2];
     float b;
+    float a;   // alpha * s[n]
     __device__ __forceinline__ void load(const EpiParams& e, int64_t n, int64_t M, int64_t N) {
         const bool use_c = e.C != nullptr && e.beta != 0.0f;
         const uint16_t* C = static_cast<const uint16_t*>(e.C);
@@ -130,9 +142,10 @@ struct EpiColumn {
         for (int m = 0; m < MN; ++m)
             if (use_c && m < M) c[m >> 1] |= static_cast<uint32_t>(C[m * N + n]) << (16 * (m & 1));
         b = e.bias != nullptr ? Elem<T>::to_float(static_cast<const T*>(e.bias)[n]) : 0.0f;
+        a = e.scale_n != nullptr ? e.alpha * e.scale_n[n] : e.alpha;
     }
     __device__ __forceinline__ float apply(const EpiParams& e, float x, int m) const {
-        x *= e.alpha;
+        x *= a;
         if (e.C != nullptr && e.beta != 0.0f)
             x += e.beta * ((m & 1) ? Elem<T>::hi(c[m >> 1]) : Elem<T>::lo(c[m >> 1]));
         if (e.bias != nullptr) x += b;

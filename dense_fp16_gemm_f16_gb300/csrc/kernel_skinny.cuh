@@ -5,7 +5,8 @@
 // "small batch leaves memory bandwidth unused" situation of the GEMM blog
 // post (section 5.4).  So the operands swap roles: each MMA is
 // tcgen05.mma M=128 (128 rows of B, i.e. 128 output columns) x N=MN (the M
-// rows of A, padded to 16/32/64 by TMA zero fill) x K=16, both operands
+// rows of A, padded to 16/32/64 by TMA zero fill) x K=16 (32 for 8-bit
+// operands), both operands
 // K-major exactly as stored.  The accumulator tile in TMEM is D^T: TMEM lane
 // = output column n, TMEM column = output row m.
 //
@@ -39,7 +40,8 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[MN]) 
     }
 }
 
-template <class Cfg, class T>
+// T is the element type of D (and C, bias); F8 selects 8-bit operands.
+template <class Cfg, class T, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const SkinnyParams p) {
@@ -90,7 +92,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
-    constexpr uint32_t idesc = ptx::idesc_kind_f16(128, MN, Elem<T>::kFormat);
+    constexpr int kStageK = stage_k(F8 ? 1 : 2);
+    const uint32_t idesc = ptx::instr_desc(128, MN, p.ab_format);
     const int64_t G = p.num_ctas;
     const int64_t W = p.units;
     const int64_t KB = p.k_blocks;
@@ -111,7 +114,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const uint64_t pol_x = ptx::policy_evict_last();
             for (int64_t u = u0; u < u1; ++u) {
                 const int64_t t = div_nonneg(u, KB);
-                const int32_t kx = static_cast<int32_t>((u - t * KB) * kBK);
+                const int32_t kx = static_cast<int32_t>((u - t * KB) * kStageK);
                 if (!wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -159,8 +162,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint64_t x_desc = ptx::sw128_kmajor_desc(sbase + Cfg::OFF_X + stage * Cfg::X_BYTES);
                     if (ptx::elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            ptx::mma_f16<1>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
+                        for (int k = 0; k < kMmaPerStage; ++k)
+                            ptx::mma<1, F8>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
                                             (u != seg_start || k != 0) ? 1u : 0u);
                         ptx::mma_commit(empty_bar(stage));
                     }

@@ -2,7 +2,8 @@
 //
 // The data path is the Blackwell one of "Building a Tiled GEMM" (MLC),
 // sections "GEMM data path" and steps 1-3: operand tiles GMEM -> SMEM
-// (128-byte swizzle, 64-wide K chunks), tcgen05.mma into a TMEM fp32
+// (128-byte swizzle, 128-byte K chunks: 64 fp16/bf16 or 128 8-bit values),
+// tcgen05.mma into a TMEM fp32
 // accumulator that stays in place across the K loop (step 2), one output tile
 // per unit of work (step 3).  Past those steps it applies the chapter's
 // optimisation roadmap ("Optimisation roadmap"): TMA loads tracked by
@@ -193,13 +194,16 @@ __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u
     return true;
 }
 
-template <class Cfg, class T>
+// T is the element type of D (and C, bias); F8 selects 8-bit operands
+// (kind::f8f6f4, 128 K elements per stage) instead of 16-bit ones of type T.
+template <class Cfg, class T, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBpiece, const __grid_constant__ CUtensorMap tmD,
                   const TiledParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int MAXS = Cfg::MAX_STAGES;
+    constexpr int kStageK = stage_k(F8 ? 1 : 2);
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1024 bytes (the 128-byte swizzle atom); every
     // CTA of a pair gets the same offsets, which the pair MMA relies on.
@@ -302,7 +306,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                     const uint32_t a_dst = sbase + stage * stride;
                     const uint32_t b_dst = a_dst + Cfg::A_BYTES;
-                    const int kx = (reverse ? (kb1 - 1 - (kb - kb0)) : kb) * kBK;
+                    const int kx = (reverse ? (kb1 - 1 - (kb - kb0)) : kb) * kStageK;
                     if (ptx::elect_one()) {
                         if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
@@ -348,7 +352,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 int64_t tm, n0;
                 int nw, kb0, kb1;
                 work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
-                const uint32_t idesc = ptx::idesc_kind_f16(Cfg::BM, nw, Elem<T>::kFormat);
+                const uint32_t idesc = ptx::instr_desc(Cfg::BM, nw, p.ab_format);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
                 if (!wait_phase_warp(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
@@ -367,8 +371,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + stage * stride + Cfg::A_BYTES);
                     if (ptx::elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            ptx::mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                        for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
+                            ptx::mma<CG, F8>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                              (kb != kb0 || k != 0) ? 1u : 0u);
                         if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
                         else ptx::mma_commit_pair(empty_bar(stage), all_mask);

@@ -32,7 +32,8 @@ struct SkinnyOps {
                           int grid_ctas, cudaStream_t stream);
 };
 
-// dtype: 0 = fp16 operands and output, 1 = bf16
+// dtype: 0 = fp16 operands and output, 1 = bf16, 2 / 3 = E4M3 / E5M2 operands
+// with a bf16 output
 const TiledOps& tiled_ops_2cta256(int dtype);
 const TiledOps& tiled_ops_4cta512(int dtype);
 const TiledOps& tiled_ops_1cta128(int dtype);

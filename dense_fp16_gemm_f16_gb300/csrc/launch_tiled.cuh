@@ -6,10 +6,10 @@
 
 namespace gemm_gb300 {
 
-template <class Cfg, class T>
+template <class Cfg, class T, bool F8>
 struct TiledLauncher {
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg::SMEM_BYTES);
     }
 
@@ -26,9 +26,9 @@ struct TiledLauncher {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg, T>, &cfg);
+            return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg, T, F8>, &cfg);
         } else {
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg, T>, kThreads,
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg, T, F8>, kThreads,
                                                                  Cfg::SMEM_BYTES);
         }
     }
@@ -55,7 +55,7 @@ struct TiledLauncher {
             cfg.numAttrs = 2;
         }
         cfg.attrs = attr;
-        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T>, a, b, b_piece, d, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T, F8>, a, b, b_piece, d, p);
     }
 
     static const TiledOps& ops() {
@@ -65,5 +65,15 @@ struct TiledLauncher {
         return o;
     }
 };
+
+// The table for a gemm_dtype_t: fp16 operands and D (0), bf16 (1), or 8-bit
+// operands (2 = E4M3, 3 = E5M2; one kernel, the format is a launch
+// parameter) with a bf16 D.
+template <class Cfg>
+const TiledOps& tiled_ops_for(int dtype) {
+    if (dtype >= 2) return TiledLauncher<Cfg, __nv_bfloat16, true>::ops();
+    if (dtype == 1) return TiledLauncher<Cfg, __nv_bfloat16, false>::ops();
+    return TiledLauncher<Cfg, __half, false>::ops();
+}
 
 }  // namespace gemm_gb300

@@ -237,6 +237,33 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
             :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// The same for 8-bit operands (E4M3 or E5M2, chosen by the instruction
+// descriptor): kind::f8f6f4, K = 32 per instruction, fp32 accumulator.
+template <int CG>
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// One MMA of either kind: 16-bit operands (kind::f16) or 8-bit (kind::f8f6f4).
+template <int CG, bool F8>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                    uint32_t accumulate) {
+    if constexpr (F8) mma_f8f6f4<CG>(d_tmem, a_desc, b_desc, idesc, accumulate);
+    else mma_f16<CG>(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
 // Arrive (once) on `bar` of this CTA when every tcgen05 operation this thread
 // issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -346,14 +373,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16: A and B both fp16
-// (format 0) or both bf16 (format 1), both K-major, fp32 accumulator, no
-// negation, dense.  M is the MMA's full M (the pair's M for cta_group::2),
-// N its N.
-//   bits  4-5   D format (1 = f32)      bits  7-9  A format (0 = f16, 1 = bf16)
+// Instruction descriptor for tcgen05.mma kind::f16 and kind::f8f6f4: A and B
+// of the same format, both K-major, fp32 accumulator, no negation, dense.
+// kind::f16 formats: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2.
+// M is the MMA's full M (the pair's M for cta_group::2), N its N.
+//   bits  4-5   D format (1 = f32)      bits  7-9  A format
 //   bits 10-12  B format (same as A)    bit  15/16 A/B major (0 = K-major)
 //   bits 17-22  N >> 3                  bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_format) {
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, uint32_t ab_format) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (0u << 15) | (0u << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }

@@ -5,10 +5,10 @@
 namespace gemm_gb300 {
 namespace {
 
-template <class Cfg, class T>
+template <class Cfg, class T, bool F8>
 struct SkinnyLauncher {
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(gemm_skinny_kernel<Cfg, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(gemm_skinny_kernel<Cfg, T, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg::SMEM_BYTES);
     }
     static cudaError_t launch(const CUtensorMap& w, const CUtensorMap& x, const SkinnyParams& p,
@@ -23,7 +23,7 @@ struct SkinnyLauncher {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 1;
         cfg.attrs = attr;
-        return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<Cfg, T>, w, x, p);
+        return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<Cfg, T, F8>, w, x, p);
     }
     static const SkinnyOps& ops() {
         static const SkinnyOps o = {Cfg::MN, Cfg::STAGES, Cfg::SMEM_BYTES, Cfg::TMEM_COLS, &prepare, &launch};
@@ -31,17 +31,19 @@ struct SkinnyLauncher {
     }
 };
 
+template <class Cfg>
+const SkinnyOps& skinny_ops_for(int dtype) {
+    if (dtype >= 2) return SkinnyLauncher<Cfg, __nv_bfloat16, true>::ops();
+    if (dtype == 1) return SkinnyLauncher<Cfg, __nv_bfloat16, false>::ops();
+    return SkinnyLauncher<Cfg, __half, false>::ops();
+}
+
 }  // namespace
 
 const SkinnyOps& skinny_ops(int mn, int dtype) {
-    if (dtype == 1) {
-        if (mn <= 16) return SkinnyLauncher<CfgSkinny16, __nv_bfloat16>::ops();
-        if (mn <= 32) return SkinnyLauncher<CfgSkinny32, __nv_bfloat16>::ops();
-        return SkinnyLauncher<CfgSkinny64, __nv_bfloat16>::ops();
-    }
-    if (mn <= 16) return SkinnyLauncher<CfgSkinny16, __half>::ops();
-    if (mn <= 32) return SkinnyLauncher<CfgSkinny32, __half>::ops();
-    return SkinnyLauncher<CfgSkinny64, __half>::ops();
+    if (mn <= 16) return skinny_ops_for<CfgSkinny16>(dtype);
+    if (mn <= 32) return skinny_ops_for<CfgSkinny32>(dtype);
+    return skinny_ops_for<CfgSkinny64>(dtype);
 }
 
 }  // namespace gemm_gb300

@@ -3,9 +3,9 @@
 
 namespace gemm_gb300 {
 const TiledOps& tiled_ops_1cta128(int dtype) {
-    return dtype == 1 ? TiledLauncher<Cfg1cta128, __nv_bfloat16>::ops() : TiledLauncher<Cfg1cta128, __half>::ops();
+    return tiled_ops_for<Cfg1cta128>(dtype);
 }
 const TiledOps& tiled_ops_1cta256(int dtype) {
-    return dtype == 1 ? TiledLauncher<Cfg1cta256, __nv_bfloat16>::ops() : TiledLauncher<Cfg1cta256, __half>::ops();
+    return tiled_ops_for<Cfg1cta256>(dtype);
 }
 }  // namespace gemm_gb300

@@ -3,6 +3,6 @@
 
 namespace gemm_gb300 {
 const TiledOps& tiled_ops_2cta256(int dtype) {
-    return dtype == 1 ? TiledLauncher<Cfg2cta256, __nv_bfloat16>::ops() : TiledLauncher<Cfg2cta256, __half>::ops();
+    return tiled_ops_for<Cfg2cta256>(dtype);
 }
 }  // namespace gemm_gb300

@@ -4,6 +4,6 @@
 
 namespace gemm_gb300 {
 const TiledOps& tiled_ops_4cta512(int dtype) {
-    return dtype == 1 ? TiledLauncher<Cfg4cta512, __nv_bfloat16>::ops() : TiledLauncher<Cfg4cta512, __half>::ops();
+    return tiled_ops_for<Cfg4cta512>(dtype);
 }
 }  // namespace gemm_gb300

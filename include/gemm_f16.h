@@ -82,11 +82,22 @@ typedef enum {
                                            loaded once per cluster and multicast to both pairs */
 } gemm_variant_t;
 
-/* Element type of A, B, D (and C, bias): both operands share it (the MMA
- * multiplies f16 by f16 or bf16 by bf16, accumulating in fp32). */
+/* Element type of A and B; both operands share it and the MMA accumulates in
+ * fp32.  D (and C, bias) is fp16 for GEMM_DTYPE_F16 and bf16 for the others.
+ * The 8-bit types are the FP8 layouts of the GEMM blog post (section 2.2), as
+ * the tensor cores define them:
+ *   E4M3  1 sign, 4 exponent (bias 7), 3 fraction bits; no infinities,
+ *         S.1111.111 is NaN; largest finite 448
+ *   E5M2  1 sign, 5 exponent (bias 15), 2 fraction bits; IEEE-like with
+ *         infinities and NaNs; largest finite 57344
+ * They are stored one byte per element.  Quantisation scales are applied in
+ * the fused epilogue: a per-tensor scale through alpha, a per-output-column
+ * (per weight row) scale through gemm_epilogue_t.scale_n. */
 typedef enum {
     GEMM_DTYPE_F16 = 0,
-    GEMM_DTYPE_BF16 = 1
+    GEMM_DTYPE_BF16 = 1,
+    GEMM_DTYPE_E4M3 = 2,
+    GEMM_DTYPE_E5M2 = 3
 } gemm_dtype_t;
 
 typedef enum {
@@ -96,16 +107,22 @@ typedef enum {
 
 /*
  * Fused output transform, applied in fp32 to the fp32 accumulator before the
- * single rounding of D:   D = act(alpha * (A B^T) + beta * C + bias[n])
+ * single rounding of D:
+ *     D = act(alpha * scale_n[n] * (A B^T) + beta * C + bias[n])
  * (the scaled update C = alpha A B + beta C and the bias/activation fusion of
- * the GEMM blog post, sections 2.1 and 5.4).
+ * the GEMM blog post, sections 2.1 and 5.4; scale_n is the per-output-channel
+ * weight scale of its 8-bit quantisation, section 4.2).
  *   alpha       scale of A B^T
  *   beta        scale of C; 0 means C is not read
  *   C           [M][N] row-major, same dtype as D, 16-byte aligned; may be D
  *               itself (in-place update) but may not partly overlap it;
  *               required when beta != 0
- *   bias        [N], same dtype, 16-byte aligned, added to every row; NULL = none
+ *   bias        [N], same dtype as D, 16-byte aligned, added to every row;
+ *               NULL = none
  *   activation  a gemm_activation_t, applied last
+ *   reserved    unused
+ *   scale_n     [N] fp32, device memory, 16-byte aligned, must not overlap D;
+ *               multiplies column n of A B^T; NULL = none.  Any dtype.
  */
 typedef struct {
     float alpha;
@@ -114,6 +131,7 @@ typedef struct {
     const void* bias;
     int32_t activation;
     int32_t reserved;
+    const float* scale_n;
 } gemm_epilogue_t;
 
 /*
@@ -157,10 +175,14 @@ GEMM_API gemm_status_t gemm_bf16_nt(const void* A, const void* B, void* D,
 /*
  * gemm_nt_ex -- the general entry point: element type, an optional fused
  * epilogue (NULL = plain D = A B^T) and the kernel variant (GEMM_VARIANT_AUTO
- * to let the planner choose).  Arguments otherwise as for gemm_f16_nt.
+ * to let the planner choose).  Arguments otherwise as for gemm_f16_nt, with
+ * A and B of `dtype` and D of the output type that dtype implies (bf16 for
+ * the 8-bit types).  For the 8-bit types K must be a multiple of 16 (rows of
+ * 16-byte units).
  * Additional errors: GEMM_ERR_INVALID_VALUE for an unknown dtype or
- * activation, beta != 0 with C == NULL, C partly overlapping D, or bias
- * overlapping D; GEMM_ERR_MISALIGNED for C or bias not 16-byte aligned.
+ * activation, beta != 0 with C == NULL, C partly overlapping D, or bias or
+ * scale_n overlapping D; GEMM_ERR_MISALIGNED for C, bias or scale_n not
+ * 16-byte aligned.
  * With K == 0 the result is act(beta * C + bias) (the empty sum is zero).
  */
 GEMM_API gemm_status_t gemm_nt_ex(gemm_dtype_t dtype, const void* A, const void* B, void* D,
@@ -211,6 +233,15 @@ typedef struct {
  */
 GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
                                int32_t num_sms, gemm_plan_t* plan);
+
+/*
+ * gemm_nt_plan_ex -- gemm_f16_nt_plan for the operand type `dtype` (what
+ * gemm_nt_ex(dtype, ...variant...) would run).  The 8-bit types move 128 K
+ * elements per pipeline stage (tile_k = 128) instead of 64.  Returns
+ * GEMM_ERR_INVALID_VALUE for an unknown dtype or a NULL plan.
+ */
+GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K,
+                                       gemm_variant_t variant, int32_t num_sms, gemm_plan_t* plan);
 
 /*
  * gemm_f16_nt_noalloc -- the small-M GEMM (M <= 64) without any device

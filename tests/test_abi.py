@@ -88,16 +88,16 @@ def test_argument_errors_are_returned_before_any_device_call(lib):
 
 
 def _call_ex(M, N, K, dtype=0, alpha=1.0, beta=0.0, C=None, bias=None, act=0, variant=0,
-             A=FAKE, B=FAKE + (1 << 32), D=FAKE + (2 << 32), epilogue=True):
+             A=FAKE, B=FAKE + (1 << 32), D=FAKE + (2 << 32), epilogue=True, scale_n=None):
     lib = g.load()
-    epi = g.Epilogue(alpha, beta, C, bias, act, 0)
+    epi = g.Epilogue(alpha, beta, C, bias, act, 0, scale_n)
     return lib.gemm_nt_ex(dtype, A, B, D, M, N, K, ctypes.byref(epi) if epilogue else None, variant, None)
 
 
 def test_epilogue_argument_errors_are_returned_before_any_device_call(lib):
     S = g.Status
     D = FAKE + (2 << 32)
-    assert _call_ex(8, 8, 8, dtype=2) == S.ERR_INVALID_VALUE            # unknown element type
+    assert _call_ex(8, 8, 8, dtype=4) == S.ERR_INVALID_VALUE            # unknown element type
     assert _call_ex(8, 8, 8, dtype=-1, epilogue=False) == S.ERR_INVALID_VALUE
     assert _call_ex(8, 8, 8, act=2) == S.ERR_INVALID_VALUE              # unknown activation
     assert _call_ex(8, 8, 8, beta=1.0) == S.ERR_INVALID_VALUE           # beta != 0 needs C
@@ -110,6 +110,20 @@ def test_epilogue_argument_errors_are_returned_before_any_device_call(lib):
     # empty problems stay a no-op with an epilogue
     assert _call_ex(0, 8, 8, beta=1.0, C=FAKE, A=0, B=0, D=0) == S.OK
     assert _call_ex(8, 0, 8, dtype=1, bias=FAKE, A=0, B=0, D=0) == S.OK
+    # per-column scales: 16-byte aligned, not inside D
+    assert _call_ex(8, 8, 8, scale_n=FAKE + (3 << 32) + 4) == S.ERR_MISALIGNED
+    assert _call_ex(8, 8, 8, scale_n=D + 64) == S.ERR_INVALID_VALUE
+    # 8-bit operands: rows of K bytes must be whole 16-byte units
+    for dt in (g.Dtype.E4M3, g.Dtype.E5M2):
+        assert _call_ex(8, 8, 8, dtype=dt) == S.ERR_MISALIGNED
+        assert _call_ex(8, 8, 40, dtype=dt, epilogue=False) == S.ERR_MISALIGNED
+        assert _call_ex(8, 12, 16, dtype=dt) == S.ERR_MISALIGNED           # D (bf16) rows
+        assert _call_ex(0, 8, 8, dtype=dt, A=0, B=0, D=0) == S.OK
+        # D may sit right after A (M x K bytes) without overlapping it
+        st = _call_ex(64, 64, 64, dtype=dt, A=FAKE, B=FAKE + 64 * 64, D=FAKE + 2 * 64 * 64, epilogue=False)
+        assert st in (S.ERR_CUDA, S.ERR_UNSUPPORTED_DEVICE, S.OK)
+        assert _call_ex(64, 64, 64, dtype=dt, A=FAKE, B=FAKE + 64 * 64, D=FAKE + 64 * 64 - 16,
+                        epilogue=False) == S.ERR_INVALID_VALUE
     # the plain bf16 entry point shares the operand checks
     assert lib.gemm_bf16_nt(FAKE + 2, FAKE + (1 << 32), D, 8, 8, 8, None) == S.ERR_MISALIGNED
     assert lib.gemm_bf16_nt(FAKE, FAKE + (1 << 32), D, 8, 8, 12, None) == S.ERR_MISALIGNED
@@ -232,6 +246,34 @@ def test_ksplit_choice(lib):
     assert q["k_split"] == 3 and q["grid_ctas"] == 2 * 20 * 3
     # AUTO splits only long K loops (>= 40 K blocks)
     assert P(256, 256, 64 * 39)["k_split"] == 1 and P(256, 256, 64 * 40)["k_split"] == 8
+
+
+def test_plans_for_8bit_operands(lib):
+    P = lambda *a, **k: g.gemm_nt_plan_ex(g.Dtype.E4M3, *a, num_sms=152, **k)  # noqa: E731
+    p = P(8192, 8192, 8192)
+    # a stage is still 128-byte rows: 128 K elements, half as many K blocks
+    assert p["variant"] == "TILE_2CTA_256x256" and (p["tile_k"], p["k_blocks"]) == (128, 64)
+    assert (p["num_full_tiles"], p["tail_split"]) == (988, 2)
+    # A rows are half as large: up to 24 tile rows per 48 MiB group, 32 rows in 2 groups of 16
+    assert p["group_m"] == 16
+    # 4112-byte rows are 16-byte units but not on 32-byte sectors (fp16 rows of
+    # 4112 elements would be): the 4-CTA clusters; 33 K blocks, the last 16 wide
+    p = P(4000, 11000, 4112)
+    assert p["variant"] == "TILE_4CTA_512x256" and p["k_blocks"] == 33 and p["group_m"] == 8
+    assert P(4000, 11000, 4128)["variant"] == "TILE_2CTA_256x256"
+    with pytest.raises(g.GemmError):
+        P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units
+    p = P(16, 8192, 8192)
+    assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and p["max_tiles_per_cta"] == 2
+    p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: split-K by 4
+    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
+    assert g.gemm_nt_plan_ex(g.Dtype.F16, 8192, 8192, 8192, num_sms=152) == \
+        g.gemm_f16_nt_plan(8192, 8192, 8192, num_sms=152)
+    assert g.gemm_nt_plan_ex(g.Dtype.E5M2, 8192, 8192, 8192, num_sms=152)["tile_k"] == 128
+    with pytest.raises(g.GemmError):
+        P(64, 64, 40)                                        # K bytes not a multiple of 16
+    with pytest.raises(g.GemmError):
+        g.gemm_nt_plan_ex(4, 64, 64, 64, num_sms=152)
 
 
 def test_plan_errors(lib):
