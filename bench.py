@@ -570,8 +570,11 @@ def run_ours(args):
         peak = FALLBACK_PEAK_TFLOPS * ratio
         peak_src = "fallback" + (" x 2 (nominal dense fp8 : bf16 ratio)" if ratio != 1.0 else "")
     achieved = metrics.tflops(w.M, w.N, w.K, launch_ms * 1e-3)
-    # the ncu counters were taken on the plain fp16 product
-    traffic = recorded_traffic(w.name) if args.dtype == "f16" and not args.epilogue else None
+    # the ncu counters were taken on the plain product (fp16), and for 8-bit
+    # operands on the product with their scales
+    traffic = None
+    if not args.epilogue:
+        traffic = recorded_traffic(w.name if args.dtype == "f16" else f"{w.name}/{args.dtype}")
     if plan["variant"] == "SKINNY_SPLITK":
         hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else 6800.0
         # algorithmic bytes: A and B read once, D written once (+ C and bias read with the

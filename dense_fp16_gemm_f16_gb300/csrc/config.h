@@ -85,7 +85,11 @@ struct TiledConfig {
     // full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2], drain
     static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;  // + slack to align the base
+    // per epilogue warp: the per-column scales (64 fp32) and bias (64 x 16 bit)
+    // of the chunk it is writing, read back by every lane as broadcasts
+    static constexpr int COLS_BYTES = EPI_COLS * 4 + EPI_COLS * 2;
+    static constexpr int OFF_COLS = (OFF_SLOT + 16 + 15) / 16 * 16;
+    static constexpr int SMEM_BYTES = OFF_COLS + kEpiWarps * COLS_BYTES + 1024;  // + slack to align the base
     static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT / PAIRS) % 1024 == 0,
                   "stage tiles (and each multicast half) must stay 1024-aligned");
     static_assert(CL == CG || (CG == 2 && CL == 4), "clusters are one pair, or two pairs");

@@ -399,6 +399,11 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int q = warp & 3;    // TMEM lanes 32q .. 32q+31 are readable by this warp
         const int ew = warp - 2;   // owner of staging buffers 2ew, 2ew+1
         const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(tempty_bar(0), leader) : tempty_bar(0);
+        // which parts of the fused transform run (warp-uniform, for the whole launch)
+        const bool epi_c = p.epi.on && p.epi.C != nullptr && p.epi.beta != 0.0f;
+        // only the column factors alpha * s[n] (the 8-bit dequantisation): a loop without branches
+        const bool epi_scale_only = p.epi.on && !epi_c && p.epi.bias == nullptr && p.epi.act == 0;
+        uint8_t* cols_area = smem + Cfg::OFF_COLS + ew * Cfg::COLS_BYTES;
         uint32_t it = 0;
         int ebuf = 0;
         for (int64_t u = cluster_idx; u < p.num_units; u += num_clusters, ++it) {
@@ -408,6 +413,15 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int chunks = nw / Cfg::EPI_COLS;
             const uint32_t buf = it & 1u;
             const uint32_t use = (it >> 1) & 1u;
+            // the per-column scales and bias of the whole unit, fetched before its
+            // accumulator is waited for (ev[0] always holds the current chunk's)
+            constexpr int kChunks = Cfg::BN / Cfg::EPI_COLS;
+            EpiCols64<T> ev[kChunks];
+            if (p.epi.on && p.ksplit == 1) {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    if (c < chunks) ev[c].load(p.epi, n0 + c * Cfg::EPI_COLS, lane, p.N);
+            }
             if (p.ksplit > 1) {
                 // all four epilogue warps decide together: they meet at named barriers
                 const bool ready = wait_phase(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
@@ -430,8 +444,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int64_t col0 = n0 + c * Cfg::EPI_COLS;
                 const bool store = rows_in && col0 < p.N;  // warp-uniform
                 // this chunk's C values, in flight while TMEM is read
-                uint4 cv[8];
-                if (p.epi.on) {
+                uint4 cv[8] = {};
+                if (epi_c) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         cv[j] = (store && col0 + 8 * j < p.N) ? epi_load_c8<T>(p.epi, row0 + lane, col0 + 8 * j, p.M, p.N)
@@ -458,17 +472,37 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     // row `lane` of the box, 16-byte chunk j at position j ^ (row % 8):
                     // the layout the 128-byte-swizzled tensor map expects
                     uint8_t* row_ptr = sb + lane * (Cfg::EPI_COLS * 2);
+                    if (p.epi.on) {
+                        ev[0].stage(cols_area, lane);
+                        __syncwarp();
+                    }
+                    if (epi_scale_only) {
+                        const float4* f4 = reinterpret_cast<const float4*>(cols_area);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float x[8];
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 s0 = f4[2 * j], s1 = f4[2 * j + 1];
+                            const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                            uint32_t h[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * j + e]);
-                        if (p.epi.on && col0 + 8 * j < p.N) epi_apply8_c<T>(p.epi, x, cv[j], col0 + 8 * j);
-                        uint32_t h[4];
+                            for (int e = 0; e < 4; ++e)
+                                h[e] = Elem<T>::pack2(__uint_as_float(v[8 * j + 2 * e]) * sc[2 * e],
+                                                      __uint_as_float(v[8 * j + 2 * e + 1]) * sc[2 * e + 1]);
+                            *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) << 4)) =
+                                make_uint4(h[0], h[1], h[2], h[3]);
+                        }
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(x[2 * e], x[2 * e + 1]);
-                        *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) << 4)) =
-                            make_uint4(h[0], h[1], h[2], h[3]);
+                        for (int j = 0; j < 8; ++j) {
+                            float x[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * j + e]);
+                            if (p.epi.on && col0 + 8 * j < p.N) epi_apply8_s<T>(p.epi, x, cv[j], epi_c, cols_area, j);
+                            uint32_t h[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(x[2 * e], x[2 * e + 1]);
+                            *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) << 4)) =
+                                make_uint4(h[0], h[1], h[2], h[3]);
+                        }
                     }
                     ptx::fence_proxy_async_smem();
                 }
@@ -480,6 +514,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     ptx::bulk_commit_group();
                 }
                 ebuf ^= 1;
+#pragma unroll
+                for (int i = 0; i + 1 < kChunks; ++i) ev[i] = ev[i + 1];
             }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
