@@ -541,6 +541,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.split = pl.tail_split;
     p.ksplit = pl.k_split;
     p.ab_format = dtype_ab_format(dtype);
+    p.last_k_steps = static_cast<int32_t>(cdiv(K * in_bytes - (pl.k_blocks - 1) * kStageRowBytes, 32));
     p.num_units = pl.k_split > 1 ? p.num_tiles * pl.k_split
                                  : pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
     p.partials = ws ? ws->partials : nullptr;

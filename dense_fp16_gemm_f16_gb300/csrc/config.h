@@ -115,6 +115,7 @@ struct TiledParams {
     int32_t split;            // the remaining tiles are cut into `split` column pieces
     int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces (split-K)
     uint32_t ab_format;       // operand format field of the MMA instruction descriptor
+    int32_t last_k_steps;     // 32-byte K steps of real data in the last K block (1..4)
     float* partials;          // split-K: [num_tiles][ksplit][BM][BN] fp32
     uint32_t* counters;       // split-K: [num_tiles], zero between calls
     void* D;                  // the output (fp16 or bf16 [M][N]); written directly by the

@@ -361,6 +361,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::BN;
+                // the producer's K order for this unit (odd rounds walk K downwards)
+                const bool reverse = (it & 1u) && p.ksplit == 1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase_warp(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                         ok = false;
@@ -369,11 +371,16 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     ptx::tc_fence_after();
                     const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + stage * stride);
                     const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + stage * stride + Cfg::A_BYTES);
+                    // the last K block holds only p.last_k_steps 32-byte steps of real
+                    // data (the rest is TMA zero fill): skip the MMAs of the others
+                    const int blk = reverse ? (kb1 - 1 - (kb - kb0)) : kb;
+                    const int steps = (blk == p.k_blocks - 1) ? p.last_k_steps : kMmaPerStage;
                     if (ptx::elect_one()) {
 #pragma unroll
                         for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
-                            ptx::mma<CG, F8>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                             (kb != kb0 || k != 0) ? 1u : 0u);
+                            if (k < steps)
+                                ptx::mma<CG, F8>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                                                 (kb != kb0 || k != 0) ? 1u : 0u);
                         if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
                         else ptx::mma_commit_pair(empty_bar(stage), all_mask);
                     }
