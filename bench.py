@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -49,7 +50,7 @@ FALLBACK_PEAK_TFLOPS = 1900.0      # used only if the measured-peaks file is abs
 L2_ROTATE_BYTES = 256 << 20        # about twice the 129 MB L2
 CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
 
 def parse_args():
@@ -186,10 +187,29 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, p in rows for i in range(4) if p[4 + i].lower() == "active"})
         power = [num(p[2]) for _, p in rows if num(p[2]) is not None]
+        mem = [num(p[8]) for _, p in rows if len(p) > 8 and num(p[8]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "mem_mhz": statistics.median(mem) if mem else None,
                 "reasons": reasons, "samples": len(rows),
                 "power_w_max": max(power) if power else None}
+
+
+def device_info(gpu_index: int) -> dict:
+    """GPU name, driver and CUDA versions of the box the line was measured on."""
+    import torch
+    info = {"gpu": torch.cuda.get_device_name(gpu_index), "cuda_runtime": torch.version.cuda,
+            "torch": torch.__version__}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,clocks.max.mem", "--format=csv,noheader,nounits",
+                              "-i", str(gpu_index)], capture_output=True, text=True, timeout=20).stdout.strip()
+        parts = [p.strip() for p in out.split(",")]
+        if len(parts) >= 2:
+            info["driver"] = parts[0]
+            info["mem_max_mhz"] = float(parts[1]) if parts[1].replace(".", "", 1).isdigit() else parts[1]
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return info
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -528,8 +548,12 @@ def run_ours(args):
     # Spread of the per-launch time: after the timed region, the same launches
     # in (up to) 30 batches with an event pair around each; reported beside the
     # value, which stays the one-region measurement above.
+    # 30 batches of at least 1 ms each (more launches per batch than steps / 30
+    # for launches under ~33 us); short diagnostic runs keep one launch per step
     batches = min(30, args.steps)
     per_batch = max(1, args.steps // batches)
+    if batches == 30:
+        per_batch = max(per_batch, math.ceil(1.0 / max(launch_ms, 1e-6)))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(batches + 1)]
     evs[0].record(stream)
     for b in range(batches):
@@ -539,7 +563,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     g.gemm_f16_nt_check(stream=stream, device=dev)
     per_launch = sorted(evs[b].elapsed_time(evs[b + 1]) / per_batch for b in range(batches))
-    spread = {"batches": batches, "launches_per_batch": per_batch,
+    spread = {"batches": batches, "launches_per_batch": per_batch, "batch_ms_min": per_launch[0] * per_batch,
               "median_ms": statistics.median(per_launch), "min_ms": per_launch[0],
               "p90_ms": per_launch[min(batches - 1, int(0.9 * batches))]}
 
@@ -618,6 +642,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "per_launch_spread": spread,
         "clocks": clocks,
+        "device": device_info(local_rank),
     }
     print(json.dumps(line), flush=True)
     if pg:

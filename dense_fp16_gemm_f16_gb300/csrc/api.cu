@@ -62,8 +62,23 @@ constexpr int64_t kMaxDim = INT32_MAX;
 // faster and 12 % less DRAM traffic than 8), 12 at 6144^3, all 16 at
 // 4000 x 11000 x 4104.  GEMM_GROUP_M fixes the group size instead.
 constexpr int64_t kL2GroupBytes = 48ll << 20;
-// AUTO uses split-K for the pair kernel only from this many K blocks up.
-constexpr int64_t kSplitKMinBlocks = 40;
+// AUTO's choice for shapes whose 256x256 tiles fill less than one round of CTA
+// pairs, from launches timed back to back on GB300 (fp16 and E4M3 alike, in
+// K blocks of one 128-byte stage each):
+//   unsplit, one tile per pair:   ~3 us + 0.25 us per K block
+//   split into S pieces:         ~14 us + 0.25 us per K block of a piece
+// (publishing and re-reading the fp32 partials is the difference), so a split
+// pays when kb * (1 - 1/S) reaches ~56 blocks.  Measured: fp16 512x2048x8192
+// (kb 128, S 4) 23.9 us split / 32.5 unsplit; fp16 1024x2048x5120 (kb 80, S 2)
+// 26.0 / 23.3; E4M3 512x2048x8192 (kb 64, S 4) 20.9 / 19.3; E4M3 768x2048x6144
+// (kb 48, S 3) 23.0 / 16.7; E4M3 512x1024x16384 (kb 128, S 8) 19.1 / 32.7.
+constexpr int64_t kSplitKSavedBlocks = 56;
+// Unsplit, the pair kernel beats 128x256 tiles on single CTAs once the K loop
+// is long enough for its halved operand traffic per FLOP to matter (fp16
+// 1024x2048x5120: 23.3 against 25.2 us; E4M3 512x2048x8192: 19.3 against
+// 19.9); short K loops favour the single CTAs (fp16 2048^3: 14.1 against
+// 15.7 us).
+constexpr int64_t kPairMinBlocks = 48;
 
 int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K, int in_bytes) {
 #ifdef GEMM_GROUP_M
@@ -140,12 +155,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // pairs and 20.3 us on 128x128; 4000x11000x4104 253 us on pairs vs
             // 350 us on 128x256.)
             // With at most half a round of pair tiles and a long K loop, split
-            // each tile's K loop over several pairs instead (fewer, larger
-            // tiles: less L2 traffic).  Publishing and re-reading the fp32
-            // partials costs a fixed ~8 us, so short K loops stay unsplit
-            // (measured on GB300: 512x2048x8192 22.9 us split vs 39.1 us on
-            // 128x256 tiles; 1024x1024x2048 15.8 us split vs 12.7 us).
+            // each tile's K loop over several pairs instead (see
+            // kSplitKSavedBlocks); unsplit, long K loops go to the pair kernel
+            // and short ones to single CTAs (kPairMinBlocks).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
+            const int64_t kb = cdiv(K, bk);
+            const int ks = choose_ksplit(t2, pairs, kb);
             // When a row of A and B (K elements) is not a whole number of 32-byte
             // sectors, the rows do not start on sectors and every 128-byte TMA row
             // reads five sectors
@@ -156,8 +171,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // level: 8192^3 641 against 656 us, K = 4112 207 against 212).
             if (t2 >= pairs)
                 variant = ((K * in_bytes) % 32 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
-            else if (cdiv(K, bk) >= kSplitKMinBlocks && choose_ksplit(t2, pairs, cdiv(K, bk)) > 1)
+            else if (ks > 1 && kb * (ks - 1) >= kSplitKSavedBlocks * ks)
                 variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
+            else if (kb >= kPairMinBlocks) variant = GEMM_VARIANT_TILE_2CTA_256x256;
             else if (cdiv(M, 128) * cdiv(N, 256) >= 2) variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else variant = GEMM_VARIANT_TILE_1CTA_128x128;
         }

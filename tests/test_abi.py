@@ -185,7 +185,7 @@ def test_plans_for_the_named_workloads(lib):
     p = P(2048, 2048, 2048)
     assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1    # 64 pair tiles: no split
     p = P(1024, 4096, 4096)
-    assert p["variant"] == "TILE_1CTA_128x256"
+    assert p["variant"] == "TILE_2CTA_256x256"                          # 64 K blocks: the pair kernel
     # split-K asked for where the tiles already fill the GPU: plain pair tiles
     p = P(8192, 8192, 8192, variant=g.Variant.TILE_2CTA_SPLITK)
     assert p["variant"] == "TILE_2CTA_256x256" and p["k_split"] == 1
@@ -244,8 +244,10 @@ def test_ksplit_choice(lib):
     assert P(256, 256, 64 * 7, variant=V)["k_split"] == 1                # under 4 K blocks per piece: no split
     q = P(256 * 4, 256 * 5, 64 * 64, variant=V)                           # 20 tiles: 3 pieces fit on 76 pairs
     assert q["k_split"] == 3 and q["grid_ctas"] == 2 * 20 * 3
-    # AUTO splits only long K loops (>= 40 K blocks)
-    assert P(256, 256, 64 * 39)["k_split"] == 1 and P(256, 256, 64 * 40)["k_split"] == 8
+    # AUTO splits only where the K blocks a split saves, kb * (1 - 1/S), reach 56
+    assert P(256, 256, 64 * 63)["k_split"] == 1 and P(256, 256, 64 * 64)["k_split"] == 8
+    assert P(1024, 2048, 64 * 80)["variant"] == "TILE_2CTA_256x256"     # S = 2 saves 40 blocks: unsplit
+    assert P(768, 2048, 64 * 96)["k_split"] == 3                          # S = 3 saves 64 blocks: split
 
 
 def test_plans_for_8bit_operands(lib):
@@ -265,8 +267,10 @@ def test_plans_for_8bit_operands(lib):
         P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units
     p = P(16, 8192, 8192)
     assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and p["max_tiles_per_cta"] == 2
-    p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: split-K by 4
-    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
+    p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: a split by 4
+    assert p["variant"] == "TILE_2CTA_256x256" and p["k_split"] == 1     # would save only 48: unsplit pairs
+    p = P(512, 1024, 16384)                                  # 128 K blocks over 8 pieces: split
+    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 8
     assert g.gemm_nt_plan_ex(g.Dtype.F16, 8192, 8192, 8192, num_sms=152) == \
         g.gemm_f16_nt_plan(8192, 8192, 8192, num_sms=152)
     assert g.gemm_nt_plan_ex(g.Dtype.E5M2, 8192, 8192, 8192, num_sms=152)["tile_k"] == 128
