@@ -611,6 +611,10 @@ def run_ours(args):
     else:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src}
+        if peaks and peaks.get("bf16_tflops_sustained"):
+            # context: the same against the measured sustained rate (seconds of
+            # back-to-back cuBLAS under the power cap), which long runs approach
+            roofline["frac_of_sustained"] = achieved / (float(peaks["bf16_tflops_sustained"]) * ratio)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
