@@ -32,6 +32,13 @@
  * pair, grows when a larger problem needs more, and keeps until the process
  * exits.  Calls on the same stream are ordered and share that workspace
  * safely; calls on different streams get different workspaces.
+ *
+ * CUDA graphs.  A call may be recorded by stream capture (and the graph
+ * replayed on new contents of the same buffers) once one uncaptured call of
+ * the same kind has run on that stream: the first call on a device sets the
+ * device up, and a call that has to grow its stream's workspace allocates
+ * (and may synchronise the stream), which a capture does not allow.  The
+ * recorded kernels keep the pointers, sizes and scalars of the captured call.
  */
 #ifndef GEMM_F16_H_
 #define GEMM_F16_H_
