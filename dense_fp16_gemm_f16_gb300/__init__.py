@@ -121,6 +121,8 @@ def load():
         lib.gemm_nt_plan_ex.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_int, ctypes.c_int32,
                                         ctypes.POINTER(Plan)]
         lib.gemm_nt_plan_ex.restype = ctypes.c_int
+        lib.gemm_selftest_timeout.argtypes = [ctypes.c_int32, p]
+        lib.gemm_selftest_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -271,6 +273,12 @@ def gemm_f16_nt_check(stream=None, device=None) -> None:
     """Synchronise ``stream`` and raise GemmError if a kernel reported a timeout."""
     handle = _stream_handle(stream, device)
     _call("gemm_f16_nt_check", (handle,), device)
+
+
+def gemm_selftest_timeout(timeout_us: int = 1000, stream=None, device=None) -> None:
+    """Enqueue the failure-detection self-test: a kernel whose bounded waits run
+    out and record a timeout; the next gemm_f16_nt_check raises it."""
+    _call("gemm_selftest_timeout", (int(timeout_us), _stream_handle(stream, device)), device)
 
 
 def gemm_f16_nt_plan(M: int, N: int, K: int, variant=Variant.AUTO, num_sms: int = 0) -> dict:

@@ -17,6 +17,7 @@
 #include "epilogue.cuh"
 #include "gemm_f16.h"
 #include "launch.h"
+#include "wait.cuh"
 
 using namespace gemm_gb300;
 
@@ -24,6 +25,22 @@ namespace {
 
 // Device status word: 0, or the first timeout any kernel recorded (see wait.cuh).
 __device__ uint32_t g_status_word;
+// A counter nothing ever increments (the failure-detection self-test waits on it).
+__device__ uint32_t g_never_set;
+
+// Failure-detection self-test: one thread waits, with the kernels' own bounded
+// waits, on an mbarrier phase that never completes and on a counter that
+// nothing increments; both give up after timeout_ns and record a timeout in
+// the status word, and the kernel returns.
+__global__ void selftest_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = ptx::smem_u32(&bar);
+    ptx::mbar_init(b, 1);
+    ptx::fence_mbar_init();
+    wait_phase(b, 0, status, kSiteSelfTest, timeout_ns);   // no arrival ever completes phase 0
+    wait_count(&g_never_set, 1, status, kSiteSelfTest, timeout_ns);
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -771,6 +788,17 @@ GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N,
         lim = limits_of(*dev);
     }
     return make_plan(M, N, K, variant, lim, plan, dtype_in_bytes(dtype));
+}
+
+GEMM_API gemm_status_t gemm_selftest_timeout(int32_t timeout_us, gemm_stream_t stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return GEMM_ERR_INVALID_VALUE;
+    DeviceState* dev = nullptr;
+    const gemm_status_t st = get_device(&dev, nullptr);
+    if (st != GEMM_OK) return st;
+    selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        dev->status, static_cast<uint64_t>(timeout_us) * 1000ull);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return GEMM_OK;
 }
 
 GEMM_API gemm_status_t gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N,

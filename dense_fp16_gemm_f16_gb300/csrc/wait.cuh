@@ -22,6 +22,7 @@ enum WaitSite : uint32_t {
     kSiteMmaDrain = 5,
     kSiteEpilogueTmemFull = 6,
     kSiteSplitPieces = 7,
+    kSiteSelfTest = 8,
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t* status, uint32_t site) {

@@ -206,6 +206,18 @@ GEMM_API gemm_status_t gemm_nt_ex(gemm_dtype_t dtype, const void* A, const void*
  */
 GEMM_API gemm_status_t gemm_f16_nt_check(gemm_stream_t stream);
 
+/*
+ * gemm_selftest_timeout -- failure-detection self-test.  Enqueues on `stream`
+ * a one-thread kernel that waits, with the same bounded waits every GEMM
+ * kernel uses, on an mbarrier phase that never completes and on a device
+ * counter that nothing increments; each wait gives up after `timeout_us`
+ * microseconds (1 .. 1000000) and records a timeout in the device status
+ * word, and the kernel returns.  The next gemm_f16_nt_check on the stream
+ * then reports GEMM_ERR_TIMEOUT and clears the word; the context stays
+ * usable.  Returns GEMM_ERR_INVALID_VALUE for a timeout out of range.
+ */
+GEMM_API gemm_status_t gemm_selftest_timeout(int32_t timeout_us, gemm_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 GEMM_API const char* gemm_status_string(gemm_status_t status);
 
