@@ -232,7 +232,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 // piece is published and the last to arrive sums the tile.
                 const bool owner = (c == c_first);
                 if (owner && etid == 0) {
-                    const uint32_t done = atomicAdd(p.counters + t, 0u);
+                    const uint32_t done = ptx::ld_acquire_gpu(p.counters + t);
                     *last_flag = (done == static_cast<uint32_t>(c_last - c_first)) ? 2u : 0u;
                 }
                 if (owner) ptx::named_bar_sync(1, 32 * kEpiWarps);
@@ -249,17 +249,15 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])),
                                                pol_keep);
-                    __threadfence();
                     ptx::named_bar_sync(1, 32 * kEpiWarps);
                     if (etid == 0) {
-                        const uint32_t prev = atomicAdd(p.counters + t, 1u);
+                        const uint32_t prev = ptx::atom_add_acq_rel_gpu(p.counters + t, 1u);
                         *last_flag = (prev == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
                     }
                     ptx::named_bar_sync(1, 32 * kEpiWarps);
                 }
                 if (*last_flag) {
                     const bool self_in_regs = (*last_flag == 2u);
-                    __threadfence();
                     if (n < p.N) {
                         EpiColumn<T, MN> ec;
                         if (p.epi.on) ec.load(p.epi, n, p.M, p.N);   // in flight during the sum

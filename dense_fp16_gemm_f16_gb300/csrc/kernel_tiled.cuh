@@ -154,17 +154,15 @@ __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u
                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
     }
-    __threadfence();
     ptx::named_bar_sync(1, 32 * kEpiWarps);
     // 2. every piece of the tile (S pieces x CG CTAs) is in
     const uint32_t pieces = static_cast<uint32_t>(S * CG);
     bool ready = true;
     if (etid == 0) {
-        atomicAdd(p.counters + t, 1u);
+        ptx::atom_add_acq_rel_gpu(p.counters + t, 1u);
         ready = wait_count(p.counters + t, pieces, p.status, kSiteSplitPieces, p.timeout_ns);
     }
     if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) return false;
-    __threadfence();
     // 3. this unit's slice of columns, summed over the pieces in ascending order.
     // The tile's BN / 8 groups of 8 columns are dealt out to the S units, so
     // every slice starts on a multiple of 8 (16-byte fp16 stores, 32-byte fp32

@@ -168,6 +168,23 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                  :: "l"(map), "r"(src), "r"(x), "r"(y) : "memory");
 }
 
+// Cross-CTA handoff of fp32 partials (split-K pieces): every thread stores its
+// partial, the CTA's threads meet at a barrier, then one thread adds to the
+// tile's counter with release semantics (its view, including the stores the
+// barrier ordered before it, becomes visible with the count) and acquire
+// semantics (the partials of the pieces counted before it become visible to
+// it, and through the next barrier to the CTA's other threads).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
