@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -106,15 +107,25 @@ def measured_peaks():
         return None
 
 
+_COMMENT = re.compile(r"/\*.*?\*/|//[^\n]*", re.S)
+
+
+def code_of(text: str) -> str:
+    """C/CUDA source with comments dropped and white space collapsed (the sources
+    hold no string literal with a comment marker)."""
+    return " ".join(_COMMENT.sub(" ", text).split())
+
+
 def source_digest() -> str:
-    """sha256 over the CUDA sources: identifies the kernel the ncu counters were taken on."""
+    """sha256 over the code of the CUDA sources (comments and layout ignored):
+    identifies the kernel the ncu counters were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_gemm_f16_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(code_of(f.read()).encode())
     return h.hexdigest()
 
 

@@ -16,7 +16,8 @@
 // is written straight to D.  A tile cut across CTAs gets one fp32 partial per
 // CTA in a workspace; the CTA that finishes last (per-tile counter) adds the
 // partials in ascending CTA order -- a fixed order, so results are bitwise
-// reproducible -- converts to fp16, writes D and re-arms the counter.
+// reproducible -- applies the fused transform if any, rounds to D's type
+// (fp16, or bf16), writes D and re-arms the counter.
 #pragma once
 
 #include <cuda_fp16.h>

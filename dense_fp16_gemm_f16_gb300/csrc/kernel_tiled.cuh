@@ -17,7 +17,8 @@
 //   warp 1             allocates / frees TMEM; in the leader CTA it issues the
 //                      MMAs (one thread issues, as step 1 of the chapter
 //                      requires) and commits them to barriers.
-//   warps 2-5          epilogue: TMEM -> registers -> fp16 -> swizzled SMEM
+//   warps 2-5          epilogue: TMEM -> registers (fused transform) -> D's
+//                      type (fp16 or bf16) -> swizzled SMEM
 //                      -> TMA store, clipped at the edges of D.
 // Warps 0 and 1 run their loops with all 32 lanes and let one elected lane
 // issue each copy, MMA and commit.  The loop's values (stage addresses,
@@ -50,7 +51,7 @@ __device__ __forceinline__ int64_t split_quad_offset(int col, int row) {
 }
 
 // Sum of the S pieces of this thread's row over columns [c_begin, c_end) (a
-// multiple of 8 wide), pieces in ascending order, written to D as fp16.
+// multiple of 8 wide), pieces in ascending order, written to D (16-bit).
 // Loads go out in batches of up to 8 float4 (two 8-column groups when S = 2,
 // else one group with up to 4 pieces) before the additions that use them.
 template <class Cfg, class T, int S>
@@ -165,7 +166,7 @@ __device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u
     if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) return false;
     // 3. this unit's slice of columns, summed over the pieces in ascending order.
     // The tile's BN / 8 groups of 8 columns are dealt out to the S units, so
-    // every slice starts on a multiple of 8 (16-byte fp16 stores, 32-byte fp32
+    // every slice starts on a multiple of 8 (16-byte stores of D, 32-byte fp32
     // loads) and the slices cover all BN columns for any S <= 8.
     constexpr int kGroups = BN / 8;
     const int c_begin = 8 * (j * kGroups / S);
