@@ -224,3 +224,28 @@ def test_identity_epilogue_is_bitwise_plain():
     g.gemm_f16_nt(dA, dB, D)
     g.gemm_f16_nt_check(device=D.device)
     assert np.array_equal(D.cpu().numpy().view(np.uint16), d_plain.view(np.uint16))
+
+
+# ---------------------------------------------------------------- per-column scale on 16-bit operands
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("variant", TILED + [g.Variant.SKINNY_SPLITK], ids=lambda v: v.name)
+def test_per_column_scale_16bit(variant, dtype):
+    # scale_n is not tied to the 8-bit types: D = act(alpha * s[n] * A·Bᵀ + beta * C + bias[n])
+    M = 40 if variant == g.Variant.SKINNY_SPLITK else 300
+    N, K = 520, 1000
+    A, B = _operands(M, N, K, dtype, seed=7100 + M)
+    rng = np.random.default_rng(7200 + M)
+    s = rng.uniform(0.25, 4.0, N).astype(np.float32)
+    C = _draw(M, N, dtype, 7300)
+    bias = _draw(1, N, dtype, 7400).reshape(N)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    dA, dB, dC, db = _dev(A, dtype), _dev(B, dtype), _dev(C, dtype), _dev(bias, dtype)
+    ds = torch.from_numpy(s).cuda()
+    for alpha, beta, with_bias, relu in [(1.0, 0.0, False, False), (0.5, -1.0, True, True)]:
+        D = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
+        g.gemm_nt_ex(dA, dB, D, alpha=alpha, beta=beta, C=dC if beta else None, bias=db if with_bias else None,
+                     activation=g.Activation.RELU if relu else g.Activation.NONE, variant=variant, scale_n=ds)
+        g.gemm_f16_nt_check(device=D.device)
+        ref = oracle.gemm_ex(A, B, dtype, alpha, beta, C if beta else None, bias if with_bias else None, relu,
+                             scale_n=s)
+        check_close(_host(D, dtype), ref, K, f"scale_n {variant.name} {dtype} alpha={alpha}", dtype=dtype, scale=4.0)
