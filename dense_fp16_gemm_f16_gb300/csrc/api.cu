@@ -96,6 +96,15 @@ constexpr int64_t kSplitKSavedBlocks = 56;
 // 19.9); short K loops favour the single CTAs (fp16 2048^3: 14.1 against
 // 15.7 us).
 constexpr int64_t kPairMinBlocks = 48;
+// Even when the pair tiles fill the GPU, K loops this short (each tile mostly
+// epilogue) run faster on 128x256 CTAs.  Interleaved A/B on GB300: E4M3 with
+// per-column scales, up to 12 K blocks, 9-12 % faster (4096x4096x1024 19.7
+// against 22.0 us on pairs, 6144x6144x1536 45.5 against 50.2, 8192x8192x512
+// 63.8 against 71.2); fp16 at 8 blocks 6-9 % faster (4096x8192x512 29.4
+// against 32.4) but at 12 blocks 2-8 % slower (6144x6144x768 46.6 against
+// 43.4), and from 16 blocks on the pairs win in both.
+constexpr int64_t kShortKBlocks16 = 8;
+constexpr int64_t kShortKBlocks8 = 12;
 
 int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K, int in_bytes) {
 #ifdef GEMM_GROUP_M
@@ -186,7 +195,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // on GB300: 4000x11000x4104 226 us against 253 us on pairs, K = 4136
             // 220 against 252; with sector-aligned rows pairs are faster or
             // level: 8192^3 641 against 656 us, K = 4112 207 against 212).
-            if (t2 >= pairs)
+            if (t2 >= pairs && kb <= (in_bytes == 1 ? kShortKBlocks8 : kShortKBlocks16))
+                variant = GEMM_VARIANT_TILE_1CTA_128x256;
+            else if (t2 >= pairs)
                 variant = ((K * in_bytes) % 32 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
             else if (ks > 1 && kb * (ks - 1) >= kSplitKSavedBlocks * ks)
                 variant = GEMM_VARIANT_TILE_2CTA_SPLITK;

@@ -280,6 +280,16 @@ def test_plans_for_8bit_operands(lib):
         g.gemm_nt_plan_ex(4, 64, 64, 64, num_sms=152)
 
 
+def test_short_k_loops_on_single_ctas(lib):
+    # pair tiles fill the GPU but each K loop is only a few blocks: 128x256 CTAs
+    F16 = lambda *a: g.gemm_f16_nt_plan(*a, num_sms=152)                  # noqa: E731
+    E4 = lambda *a: g.gemm_nt_plan_ex(g.Dtype.E4M3, *a, num_sms=152)      # noqa: E731
+    assert F16(4096, 8192, 512)["variant"] == "TILE_1CTA_128x256"          # 8 blocks
+    assert F16(6144, 6144, 768)["variant"] == "TILE_2CTA_256x256"          # 12 blocks
+    assert E4(6144, 6144, 1536)["variant"] == "TILE_1CTA_128x256"          # 12 blocks of 128
+    assert E4(4096, 4096, 2048)["variant"] == "TILE_2CTA_256x256"          # 16 blocks
+
+
 def test_plan_errors(lib):
     with pytest.raises(g.GemmError):
         g.gemm_f16_nt_plan(-1, 8, 8, num_sms=152)
