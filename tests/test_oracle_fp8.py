@@ -199,3 +199,19 @@ def test_planted_mistakes_are_caught(name, tmp_path):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake {name!r}"
+
+
+def test_format_bounds_printed_by_the_pages(oracle_impl):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "fp8_quantisation_bounds.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert [r[0] for r in rows] == ["e4m3", "e5m2"]
+    for fmt, ebits, mbits, top in rows:
+        codes = np.arange(256, dtype=np.uint8)
+        vals = (oracle_impl.e4m3_to_f64 if fmt == "e4m3" else oracle_impl.e5m2_to_f64)(codes)
+        finite = vals[np.isfinite(vals)]
+        assert finite.max() == float(top) and finite.min() == -float(top), fmt
+        # the layout: 1 + ebits + mbits bits; 2^mbits values per binade above the subnormals
+        assert 1 + int(ebits) + int(mbits) == 8
+        one = list(vals).index(1.0)
+        assert vals[one + 1] - 1.0 == 2.0 ** -int(mbits), fmt
