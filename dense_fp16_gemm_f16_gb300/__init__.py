@@ -41,7 +41,6 @@ class Variant(enum.IntEnum):
     TILE_1CTA_128x256 = 3
     SKINNY_SPLITK = 4
     TILE_2CTA_SPLITK = 5
-    TILE_4CTA_512x256 = 6
 
 
 class Dtype(enum.IntEnum):

@@ -53,7 +53,6 @@ struct DeviceState {
     int sms = 0;
     uint32_t* status = nullptr;
     int max_clusters_2cta = 0;   // co-resident 2-CTA clusters of the 256x256 kernel
-    int max_clusters_4cta = 0;   // co-resident 4-CTA clusters of the 512x256 kernel
     int per_sm_1cta128 = 0;      // co-resident CTAs per SM
     int per_sm_1cta256 = 0;
 };
@@ -142,7 +141,6 @@ uint32_t dtype_ab_format(int dtype) {
 struct Limits {
     int sms;
     int max_clusters_2cta;
-    int max_clusters_4cta;
     int per_sm_1cta128;
     int per_sm_1cta256;
 };
@@ -154,7 +152,6 @@ const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
     switch (v) {
         case GEMM_VARIANT_TILE_1CTA_128x128: return tiled_ops_1cta128(dtype);
         case GEMM_VARIANT_TILE_1CTA_128x256: return tiled_ops_1cta256(dtype);
-        case GEMM_VARIANT_TILE_4CTA_512x256: return tiled_ops_4cta512(dtype);
         default: return tiled_ops_2cta256(dtype);   // TILE_2CTA_256x256, TILE_2CTA_SPLITK
     }
 }
@@ -165,7 +162,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     const gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
     const int64_t bk = stage_k(in_bytes);
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
     const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
@@ -187,18 +184,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
             const int64_t kb = cdiv(K, bk);
             const int ks = choose_ksplit(t2, pairs, kb);
-            // When a row of A and B (K elements) is not a whole number of 32-byte
-            // sectors, the rows do not start on sectors and every 128-byte TMA row
-            // reads five sectors
-            // instead of four; then the 4-CTA clusters, which fetch each B block
-            // once for two pairs, win despite using 144 of the 152 SMs (measured
-            // on GB300: 4000x11000x4104 226 us against 253 us on pairs, K = 4136
-            // 220 against 252; with sector-aligned rows pairs are faster or
-            // level: 8192^3 641 against 656 us, K = 4112 207 against 212).
             if (t2 >= pairs && kb <= (in_bytes == 1 ? kShortKBlocks8 : kShortKBlocks16))
                 variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else if (t2 >= pairs)
-                variant = ((K * in_bytes) % 32 != 0) ? GEMM_VARIANT_TILE_4CTA_512x256 : GEMM_VARIANT_TILE_2CTA_256x256;
+                variant = GEMM_VARIANT_TILE_2CTA_256x256;
             else if (ks > 1 && kb * (ks - 1) >= kSplitKSavedBlocks * ks)
                 variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
             else if (kb >= kPairMinBlocks) variant = GEMM_VARIANT_TILE_2CTA_256x256;
@@ -254,9 +243,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     const int64_t tiles = pl->m_tiles * pl->n_tiles;
     // slots = clusters (or CTAs) that can be resident at once
     int64_t slots;
-    if (ops.cluster == 4) {
-        slots = lim.max_clusters_4cta > 0 ? lim.max_clusters_4cta : lim.sms / 4;
-    } else if (ops.cta_group == 2) {
+    if (ops.cta_group == 2) {
         slots = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
     } else {
         const int per_sm = variant == GEMM_VARIANT_TILE_1CTA_128x128 ? lim.per_sm_1cta128 : lim.per_sm_1cta256;
@@ -324,24 +311,21 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
         }
         const TiledOps* tiled[3] = {&tiled_ops_2cta256(0), &tiled_ops_1cta128(0), &tiled_ops_1cta256(0)};
         for (int dt : {0, 1, 2}) {   // fp16, bf16, 8-bit (one kernel for both formats)
-            const TiledOps* all[4] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt),
-                                      &tiled_ops_4cta512(dt)};
+            const TiledOps* all[3] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt)};
             for (const TiledOps* t : all)
                 if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
             for (int mn : {16, 32, 64})
                 if (skinny_ops(mn, dt).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
         }
         int clusters = 0, per128 = 0, per256 = 0;
-        int clusters4 = 0;
         if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
-            tiled[2]->max_active(&per256) != cudaSuccess || tiled_ops_4cta512(0).max_active(&clusters4) != cudaSuccess) {
+            tiled[2]->max_active(&per256) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         d.sms = sms;
         d.status = static_cast<uint32_t*>(status);
         d.max_clusters_2cta = clusters;
-        d.max_clusters_4cta = clusters4;
         d.per_sm_1cta128 = per128;
         d.per_sm_1cta256 = per256;
         d.ready = true;
@@ -352,7 +336,7 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    return Limits{d.sms, d.max_clusters_2cta, d.max_clusters_4cta, d.per_sm_1cta128, d.per_sm_1cta256};
+    return Limits{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256};
 }
 
 // 2-D tensor map of a gemm_dtype_t's elements (fp16, bf16, or bytes for the
@@ -485,7 +469,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
             if (epi.scale_n && ranges_overlap(epi.scale_n, N * 4, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_4CTA_512x256) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
@@ -776,7 +760,7 @@ GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_va
     if (plan == nullptr) return GEMM_ERR_INVALID_VALUE;
     Limits lim;
     if (num_sms > 0) {
-        lim = Limits{num_sms, num_sms / 2, num_sms / 4, 1, 1};
+        lim = Limits{num_sms, num_sms / 2, 1, 1};
     } else {
         DeviceState* dev = nullptr;
         const gemm_status_t st = get_device(&dev, nullptr);
@@ -791,7 +775,7 @@ GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N,
     if (plan == nullptr || !dtype_valid(dtype)) return GEMM_ERR_INVALID_VALUE;
     Limits lim;
     if (num_sms > 0) {
-        lim = Limits{num_sms, num_sms / 2, num_sms / 4, 1, 1};
+        lim = Limits{num_sms, num_sms / 2, 1, 1};
     } else {
         DeviceState* dev = nullptr;
         const gemm_status_t st = get_device(&dev, nullptr);

@@ -51,20 +51,13 @@ GEMM_HD int64_t div_nonneg(int64_t a, int64_t b) {
 // cta_group::2 pair in a 2-CTA cluster), BN = output columns per tile.  A tile
 // is BM = 128*CG rows by BN columns; each CTA of a pair loads its own 128 rows
 // of A and its own BN/CG rows of B and owns 128 accumulator rows in its TMEM.
-// CL = CTAs per cluster: CG, or 4 for two pairs that work on vertically
-// adjacent tiles (same B columns) and share each B block: each CTA loads half
-// of its B rows and multicasts them to itself and to its counterpart in the
-// other pair, halving the B traffic from L2.  A unit of work is then a
-// cluster tile of PAIRS * BM rows.
-template <int CG_, int BN_, int STAGES_, int CL_ = CG_>
+// Reuse of A and B blocks between tiles comes from L2 (grouped raster below).
+template <int CG_, int BN_, int STAGES_>
 struct TiledConfig {
     static constexpr int CG = CG_;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
-    static constexpr int CL = CL_;
-    static constexpr int PAIRS = CL / CG;                     // MMA groups per cluster
     static constexpr int BM = 128 * CG;
-    static constexpr int UNIT_M = BM * PAIRS;                 // rows of a cluster tile
     static constexpr int A_ROWS = 128;
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = A_ROWS * kStageRowBytes;
@@ -90,9 +83,7 @@ struct TiledConfig {
     static constexpr int COLS_BYTES = EPI_COLS * 4 + EPI_COLS * 2;
     static constexpr int OFF_COLS = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int SMEM_BYTES = OFF_COLS + kEpiWarps * COLS_BYTES + 1024;  // + slack to align the base
-    static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT / PAIRS) % 1024 == 0,
-                  "stage tiles (and each multicast half) must stay 1024-aligned");
-    static_assert(CL == CG || (CG == 2 && CL == 4), "clusters are one pair, or two pairs");
+    static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT) % 1024 == 0, "stage tiles must stay 1024-aligned");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 up to 256");
     static_assert(B_ROWS <= 256, "TMA box rows are limited to 256");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
@@ -100,7 +91,6 @@ struct TiledConfig {
 };
 
 using Cfg2cta256 = TiledConfig<2, 256, 6>;
-using Cfg4cta512 = TiledConfig<2, 256, 6, 4>;   // two pairs sharing B: 512 x 256 per cluster
 using Cfg1cta128 = TiledConfig<1, 128, 6>;
 using Cfg1cta256 = TiledConfig<1, 256, 4>;
 

@@ -212,17 +212,11 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // rank = this CTA's rank in its MMA pair; pair = which pair of the cluster;
-    // leader = cluster rank of the pair's first CTA (it issues the MMAs)
-    constexpr int PAIRS = Cfg::PAIRS;
-    const uint32_t crank = (Cfg::CL > 1) ? ptx::cluster_ctarank() : 0u;
-    const uint32_t rank = crank % CG;
-    const uint32_t pair = crank / CG;
-    const uint32_t leader = pair * CG;
-    // commits that free a stage reach every CTA that writes into it: with B
-    // shared between the pairs, that is the whole cluster
-    const uint16_t all_mask = static_cast<uint16_t>((1u << Cfg::CL) - 1u);
-    const uint16_t pair_mask = static_cast<uint16_t>(((1u << CG) - 1u) << leader);
+    // rank = this CTA's rank in its MMA pair (the cluster); rank 0 leads:
+    // it issues the MMAs, which commit to barriers in both CTAs
+    const uint32_t rank = (CG > 1) ? ptx::cluster_ctarank() : 0u;
+    constexpr uint32_t leader = 0;
+    const uint16_t pair_mask = static_cast<uint16_t>((1u << CG) - 1u);
 
     const uint32_t bar0 = sbase + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -242,7 +236,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         ptx::prefetch_tensormap(&tmD);
         for (int s = 0; s < MAXS; ++s) {
             ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival + TMA bytes
-            ptx::mbar_init(empty_bar(s), PAIRS);  // one MMA commit per pair reading it
+            ptx::mbar_init(empty_bar(s), 1);   // one MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);                 // one MMA commit
@@ -266,8 +260,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
-    const int64_t cluster_idx = blockIdx.x / Cfg::CL;
-    const int64_t num_clusters = gridDim.x / Cfg::CL;
+    const int64_t cluster_idx = blockIdx.x / CG;
+    const int64_t num_clusters = gridDim.x / CG;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -290,10 +284,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // each CTA of a pair supplies nw / CG rows of B to the MMA; a
                 // column piece of a tail tile loads only those rows (box of the
                 // second B map) instead of the whole tile's
-                const int32_t a_row = static_cast<int32_t>((tm * PAIRS + pair) * Cfg::BM + rank * Cfg::A_ROWS);
-                // with two pairs, this CTA loads the pair-th half of its B rows and
-                // multicasts it to the same CTA rank of both pairs
-                const int32_t b_row = static_cast<int32_t>(n0 + rank * (nw / CG) + pair * (nw / CG / PAIRS));
+                const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * Cfg::A_ROWS);
+                const int32_t b_row = static_cast<int32_t>(n0 + rank * (nw / CG));
                 const bool piece = nw < Cfg::BN;
                 const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
                 const uint32_t stage_bytes = Cfg::A_BYTES + (piece ? Cfg::B_BYTES / p.split : Cfg::B_BYTES);
@@ -317,13 +309,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             const uint32_t leader_full = ptx::mapa(full_bar(stage), leader);
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
                             ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kx, a_row);
-                            if constexpr (PAIRS == 1) {
-                                ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kx, b_row);
-                            } else {
-                                const uint32_t half = (stage_bytes - Cfg::A_BYTES) / PAIRS;
-                                ptx::tma_load_2d_pair_mc(b_dst + pair * half, b_map, leader_full, kx, b_row,
-                                                         static_cast<uint16_t>((1u << rank) | (1u << (rank + CG))));
-                            }
+                            ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kx, b_row);
                         }
                     }
                     __syncwarp();
@@ -381,7 +367,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 ptx::mma<CG, F8>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                                  (kb != kb0 || k != 0) ? 1u : 0u);
                         if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
-                        else ptx::mma_commit_pair(empty_bar(stage), all_mask);
+                        else ptx::mma_commit_pair(empty_bar(stage), pair_mask);
                     }
                     __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -436,7 +422,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             ptx::tc_fence_after();
-            const int64_t row0 = (tm * PAIRS + pair) * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
+            const int64_t row0 = tm * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
             const bool rows_in = row0 < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
             if (p.ksplit > 1) {

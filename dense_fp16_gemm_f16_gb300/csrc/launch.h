@@ -11,9 +11,8 @@
 namespace gemm_gb300 {
 
 struct TiledOps {
-    // tile_m: rows of one unit of work (a cluster tile); cluster: CTAs per cluster;
-    // b_box_rows: rows of B per TMA box (each CTA's B rows, or half of them when
-    // two pairs share B)
+    // tile_m: rows of one tile (per CTA pair when cta_group == 2); cluster: CTAs
+    // per cluster; b_box_rows: rows of B per TMA box (each CTA's B rows)
     int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols, cluster, b_box_rows;
     // set the kernel's shared-memory limit on the current device
     cudaError_t (*prepare)();
@@ -35,7 +34,6 @@ struct SkinnyOps {
 // dtype: 0 = fp16 operands and output, 1 = bf16, 2 / 3 = E4M3 / E5M2 operands
 // with a bf16 output
 const TiledOps& tiled_ops_2cta256(int dtype);
-const TiledOps& tiled_ops_4cta512(int dtype);
 const TiledOps& tiled_ops_1cta128(int dtype);
 const TiledOps& tiled_ops_1cta256(int dtype);
 const SkinnyOps& skinny_ops(int mn, int dtype);  // mn = 16, 32 or 64

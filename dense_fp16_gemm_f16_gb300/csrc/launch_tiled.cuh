@@ -14,14 +14,14 @@ struct TiledLauncher {
     }
 
     static cudaError_t max_active(int* out) {
-        if constexpr (Cfg::CL > 1) {
+        if constexpr (Cfg::CG > 1) {
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(Cfg::CL, 1, 1);
+            cfg.gridDim = dim3(Cfg::CG, 1, 1);
             cfg.blockDim = dim3(kThreads, 1, 1);
             cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = Cfg::CL;
+            attr[0].val.clusterDim.x = Cfg::CG;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
@@ -47,9 +47,9 @@ struct TiledLauncher {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 1;
-        if constexpr (Cfg::CL > 1) {
+        if constexpr (Cfg::CG > 1) {
             attr[1].id = cudaLaunchAttributeClusterDimension;
-            attr[1].val.clusterDim.x = Cfg::CL;
+            attr[1].val.clusterDim.x = Cfg::CG;
             attr[1].val.clusterDim.y = 1;
             attr[1].val.clusterDim.z = 1;
             cfg.numAttrs = 2;
@@ -59,8 +59,8 @@ struct TiledLauncher {
     }
 
     static const TiledOps& ops() {
-        static const TiledOps o = {Cfg::CG, Cfg::UNIT_M, Cfg::BN, Cfg::STAGES, Cfg::SMEM_BYTES,
-                                   Cfg::TMEM_COLS, Cfg::CL, Cfg::B_ROWS / Cfg::PAIRS,
+        static const TiledOps o = {Cfg::CG, Cfg::BM, Cfg::BN, Cfg::STAGES, Cfg::SMEM_BYTES,
+                                   Cfg::TMEM_COLS, Cfg::CG, Cfg::B_ROWS,
                                    &prepare, &max_active, &launch};
         return o;
     }

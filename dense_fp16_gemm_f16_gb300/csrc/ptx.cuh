@@ -149,18 +149,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         :: "r"(dst), "l"(map), "r"(bar_cluster), "r"(x), "r"(y) : "memory");
 }
 
-// The pair load multicast to the CTAs of cta_mask: the data lands at the same
-// offset in each of them, and each one's byte count completes on the barrier
-// at bar's offset in the leader CTA of that CTA's pair (bar is given with the
-// pair bit clear).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        :: "r"(dst), "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask) : "memory");
-}
-
 // 2-D tiled store from shared memory; the box is clipped at the tensor edges.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y) {

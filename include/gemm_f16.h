@@ -83,10 +83,7 @@ typedef enum {
     GEMM_VARIANT_TILE_2CTA_SPLITK = 5   /* 2-CTA 256x256 tiles with each tile's K loop split over
                                            several CTA pairs (for shapes with few tiles); falls
                                            back to GEMM_VARIANT_TILE_2CTA_256x256 when the tiles
-                                           already fill the GPU */,
-    GEMM_VARIANT_TILE_4CTA_512x256 = 6  /* persistent, 4-CTA clusters of two 2-CTA pairs on
-                                           vertically adjacent 256x256 tiles; each B block is
-                                           loaded once per cluster and multicast to both pairs */
+                                           already fill the GPU */
 } gemm_variant_t;
 
 /* Element type of A and B; both operands share it and the MMA accumulates in

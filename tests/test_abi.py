@@ -161,17 +161,12 @@ def test_plans_for_the_named_workloads(lib):
     # at most 12 tile rows (12 x 256 rows x 16 KB = 48 MiB of A) per group: 32 rows in 3 groups of 11
     assert p["group_m"] == 11
     p = P(4000, 11000, 4104)
-    # K = 4104 is not a multiple of 64 (rows not on 128-byte lines): 4-CTA
-    # clusters of two pairs sharing B, 512 x 256 per cluster
-    assert p["variant"] == "TILE_4CTA_512x256" and p["grid_ctas"] % 4 == 0
-    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (8, 43, 65)    # ragged in M, N and K
-    assert (p["num_full_tiles"], p["tail_split"]) == (342, 4)           # 9 rounds of 38 + 2 tiles in quarters
-    assert p["group_m"] == 8                                            # all of A (32 MiB) in one group
-    # rows on 32-byte sectors (K a multiple of 16): the pair kernel, on all 152 SMs
+    # the pair kernel on all 152 SMs, ragged in M, N and K (the last K block 8 wide)
+    assert p["variant"] == "TILE_2CTA_256x256" and p["grid_ctas"] == 152
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)
+    assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds of 76 + 4 tiles in quarters
+    assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
     assert P(4000, 11000, 4112)["variant"] == "TILE_2CTA_256x256"
-    assert P(4000, 11000, 4136)["variant"] == "TILE_4CTA_512x256"
-    q = P(4000, 11000, 4104, variant=g.Variant.TILE_2CTA_256x256)       # the pair kernel on request
-    assert (q["m_tiles"], q["num_full_tiles"], q["tail_split"]) == (16, 684, 4)
     p = P(1024, 1024, 2048)
     # 16 pair tiles but a short K loop (32 blocks): 128x256 tiles in quarters
     assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1
@@ -258,10 +253,9 @@ def test_plans_for_8bit_operands(lib):
     assert (p["num_full_tiles"], p["tail_split"]) == (988, 2)
     # A rows are half as large: up to 24 tile rows per 48 MiB group, 32 rows in 2 groups of 16
     assert p["group_m"] == 16
-    # 4112-byte rows are 16-byte units but not on 32-byte sectors (fp16 rows of
-    # 4112 elements would be): the 4-CTA clusters; 33 K blocks, the last 16 wide
+    # 4112-byte rows: 33 K blocks, the last 16 wide; all of A (16 MiB) in one raster group
     p = P(4000, 11000, 4112)
-    assert p["variant"] == "TILE_4CTA_512x256" and p["k_blocks"] == 33 and p["group_m"] == 8
+    assert p["variant"] == "TILE_2CTA_256x256" and p["k_blocks"] == 33 and p["group_m"] == 16
     assert P(4000, 11000, 4128)["variant"] == "TILE_2CTA_256x256"
     with pytest.raises(g.GemmError):
         P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units
