@@ -41,6 +41,7 @@ class Variant(enum.IntEnum):
     TILE_1CTA_128x256 = 3
     SKINNY_SPLITK = 4
     TILE_2CTA_SPLITK = 5
+    SKINNY_STREAMK = 6
 
 
 class Dtype(enum.IntEnum):

@@ -55,6 +55,7 @@ struct DeviceState {
     int max_clusters_2cta = 0;   // co-resident 2-CTA clusters of the 256x256 kernel
     int per_sm_1cta128 = 0;      // co-resident CTAs per SM
     int per_sm_1cta256 = 0;
+    int skinny_clusters[kSkinnyMaxPieces + 1] = {};   // co-resident small-M clusters of P CTAs
 };
 
 struct Workspace {
@@ -143,7 +144,77 @@ struct Limits {
     int max_clusters_2cta;
     int per_sm_1cta128;
     int per_sm_1cta256;
+    int skinny_clusters[kSkinnyMaxPieces + 1];   // index P: co-resident clusters of P CTAs (0: unknown)
 };
+
+// A pure-host planner's view of a GPU with `sms` SMs (nothing queried).
+Limits host_limits(int sms) {
+    Limits lim{sms, sms / 2, 1, 1, {}};
+    for (int pc = 1; pc <= kSkinnyMaxPieces; pc *= 2) lim.skinny_clusters[pc] = sms / pc;
+    return lim;
+}
+
+// Column ranges x K pieces of the small-M kernel (kernel_skinny.cuh).  For P
+// in {1, 2, 4, 8} pieces per range: with P > 1 one range per cluster and all
+// clusters resident at once, R = min(SMs / P, resident clusters, N) ranges,
+// and R must reach ceil(N / 128) (ranges of at most 128 columns); with P = 1
+// ranges are dealt to at most one CTA per SM, in as many rounds as needed.
+// Each choice is timed with a simple model and the fastest wins (ties keep
+// the smaller P).  A CTA runs rounds * ceil(kb / P) ring stages and moves
+// (width + M) rows of 128 bytes per stage (its B rows and A's M rows); it
+// takes the longer of those bytes at its share of HBM bandwidth and its
+// stages at one per kSkinnyStageUs, plus the in-cluster sum when P > 1.
+// Measured on GB300 (all P forced in turn): a CTA finishes at most about one
+// stage per 0.25 us however narrow its B slot (the four MMAs of a stage and
+// their barrier round trip), so narrow ranges are stage-bound and lose to
+// wider ones split over a cluster -- e.g. 1 x 8192 x 8192: 152 ranges of 54
+// columns 31.4 us, 76 ranges of 108 columns in pairs 21.6 us.
+constexpr double kSkinnyHbmBytesPerUs = 6.7e6;
+constexpr double kSkinnyStageUs = 0.25;
+constexpr double kSkinnyExchangeUs = 0.5;
+
+struct SkinnyShape {
+    int pieces;
+    int64_t ranges, width, rounds, grid;
+};
+
+SkinnyShape plan_skinny(int64_t M, int64_t N, int64_t kb, const Limits& lim) {
+    const int64_t G = lim.sms;
+    const int64_t r_min = cdiv(N, 128);
+    SkinnyShape best{1, 0, 0, 0, 0};
+    double best_t = 0.0;
+    for (int pc = 1; pc <= kSkinnyMaxPieces; pc *= 2) {
+        if (pc > kb) break;
+#ifdef GEMM_SKINNY_PIECES
+        // a build that fixes P (where the shape allows it), for measurements
+        if (pc != GEMM_SKINNY_PIECES && best.ranges != 0) continue;
+#endif
+        SkinnyShape sh{pc, 0, 0, 1, 0};
+        if (pc == 1) {
+            sh.rounds = cdiv(r_min, G);
+            sh.ranges = std::min<int64_t>(sh.rounds * G, N);
+            sh.grid = std::min<int64_t>(sh.ranges, G);
+        } else {
+            const int64_t cap = std::min<int64_t>(G / pc, lim.skinny_clusters[pc]);
+            if (cap < r_min) continue;
+            sh.ranges = std::min<int64_t>(cap, N);
+            sh.grid = sh.ranges * pc;
+        }
+        sh.width = cdiv(N, sh.ranges);
+        const double stages = static_cast<double>(sh.rounds * cdiv(kb, pc));
+        const double bytes = stages * static_cast<double>((sh.width + M) * kStageRowBytes);
+        double t = std::max(bytes * static_cast<double>(sh.grid) / kSkinnyHbmBytesPerUs, stages * kSkinnyStageUs) +
+                   (pc > 1 ? kSkinnyExchangeUs : 0.0);
+#ifdef GEMM_SKINNY_PIECES
+        if (pc == GEMM_SKINNY_PIECES) t = -1.0;
+#endif
+        if (best.ranges == 0 || t < best_t - 1e-9) {
+            best = sh;
+            best_t = t;
+        }
+    }
+    return best;
+}
 
 int skinny_mn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
@@ -162,8 +233,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     const gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
     const int64_t bk = stage_k(in_bytes);
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
-    if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_STREAMK) return GEMM_ERR_INVALID_VALUE;
+    if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
+        return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
     const int64_t pairs = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
 
@@ -202,6 +274,30 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     if (variant == GEMM_VARIANT_SKINNY_SPLITK) {
         const int mn = skinny_mn(M);
         const SkinnyOps& ops = skinny_ops(mn, 0);
+        pl->cta_group = 1;
+        pl->tile_m = mn;
+        pl->stages = std::min(ops.max_stages, ops.ring_bytes / (skinny_w_stride(128) + ops.x_bytes));
+        pl->smem_bytes = ops.smem_bytes;
+        pl->tmem_cols = ops.tmem_cols;
+        pl->m_tiles = 1;
+        pl->tile_n = 128;
+        pl->n_tiles = cdiv(N, 128);
+        if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+        const SkinnyShape sh = plan_skinny(M, N, pl->k_blocks, lim);
+        pl->tile_n = static_cast<int32_t>(sh.width);
+        // ring stages of B slots sized to the range width (narrow ranges get more)
+        pl->stages = std::min(ops.max_stages, ops.ring_bytes / (skinny_w_stride(pl->tile_n) + ops.x_bytes));
+        pl->n_tiles = sh.ranges;
+        pl->k_split = sh.pieces;
+        pl->grid_ctas = static_cast<int32_t>(sh.grid);
+        pl->max_tiles_per_cta = static_cast<int32_t>(sh.rounds);
+        pl->workspace_bytes = 0;
+        return GEMM_OK;
+    }
+
+    if (variant == GEMM_VARIANT_SKINNY_STREAMK) {
+        const int mn = skinny_mn(M);
+        const StreamKOps& ops = streamk_ops(mn, 0);
         pl->cta_group = 1;
         pl->tile_m = mn;
         pl->tile_n = 128;
@@ -315,7 +411,10 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
             for (const TiledOps* t : all)
                 if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
             for (int mn : {16, 32, 64})
-                if (skinny_ops(mn, dt).prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+                if (skinny_ops(mn, dt).prepare() != cudaSuccess || streamk_ops(mn, dt).prepare() != cudaSuccess) {
+                    cudaGetLastError();
+                    return GEMM_ERR_CUDA;
+                }
         }
         int clusters = 0, per128 = 0, per256 = 0;
         if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
@@ -328,6 +427,13 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
         d.max_clusters_2cta = clusters;
         d.per_sm_1cta128 = per128;
         d.per_sm_1cta256 = per256;
+        d.skinny_clusters[1] = sms;
+        for (int pc = 2; pc <= kSkinnyMaxPieces; pc *= 2) {
+            if (skinny_ops(16, 0).max_active(pc, &d.skinny_clusters[pc]) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+        }
         d.ready = true;
     }
     *out = &d;
@@ -336,7 +442,9 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    return Limits{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256};
+    Limits lim{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256, {}};
+    for (int pc = 1; pc <= kSkinnyMaxPieces; ++pc) lim.skinny_clusters[pc] = d.skinny_clusters[pc];
+    return lim;
 }
 
 // 2-D tensor map of a gemm_dtype_t's elements (fp16, bf16, or bytes for the
@@ -469,8 +577,9 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
             if (epi.scale_n && ranges_overlap(epi.scale_n, N * 4, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
-    if (variant == GEMM_VARIANT_SKINNY_SPLITK && M > 64) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_STREAMK) return GEMM_ERR_INVALID_VALUE;
+    if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
+        return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     if (D == nullptr) return GEMM_ERR_INVALID_VALUE;
     if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
@@ -511,6 +620,35 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     if (pl.variant == GEMM_VARIANT_SKINNY_SPLITK) {
         const SkinnyOps& ops = skinny_ops(pl.tile_m, dtype);
         CUtensorMap tw, tx;
+        if (!encode_2d(&tw, B, K, N, bk, static_cast<uint32_t>(pl.tile_n), dtype) ||
+            !encode_2d(&tx, A, K, M, bk, static_cast<uint32_t>(ops.mn), dtype))
+            return GEMM_ERR_INVALID_VALUE;
+        SkinnyParams p;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.k_blocks = static_cast<int32_t>(pl.k_blocks);
+        p.width = pl.tile_n;
+        p.ranges = static_cast<int32_t>(pl.n_tiles);
+        p.pieces = pl.k_split;
+        p.stages = pl.stages;
+        p.w_stride = skinny_w_stride(pl.tile_n);
+        p.D = D;
+        p.epi = epi;
+        p.status = dev->status;
+        p.timeout_ns = timeout_for(pl.k_blocks);
+        p.stream_b = b_bytes >= kStreamBBytes ? 1 : 0;
+        p.ab_format = dtype_ab_format(dtype);
+        if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+
+    if (pl.variant == GEMM_VARIANT_SKINNY_STREAMK) {
+        const StreamKOps& ops = streamk_ops(pl.tile_m, dtype);
+        CUtensorMap tw, tx;
         if (!encode_2d(&tw, B, K, N, bk, 128, dtype) ||
             !encode_2d(&tx, A, K, M, bk, static_cast<uint32_t>(ops.mn), dtype))
             return GEMM_ERR_INVALID_VALUE;
@@ -518,7 +656,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
         st = get_workspace(dev_id, stream, partial_bytes, static_cast<size_t>(pl.n_tiles), &ws);
         if (st != GEMM_OK) return st;
-        SkinnyParams p;
+        StreamKParams p;
         p.M = static_cast<int32_t>(M);
         p.N = static_cast<int32_t>(N);
         p.K = static_cast<int32_t>(K);
@@ -639,9 +777,9 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
     }
 
     gemm_plan_t pl;
-    st = make_plan(M, N, K, GEMM_VARIANT_SKINNY_SPLITK, limits_of(*dev), &pl);
+    st = make_plan(M, N, K, GEMM_VARIANT_SKINNY_STREAMK, limits_of(*dev), &pl);
     if (st != GEMM_OK) return st;
-    const SkinnyOps& ops = skinny_ops(pl.tile_m, 0);
+    const StreamKOps& ops = streamk_ops(pl.tile_m, 0);
     const size_t counter_bytes = static_cast<size_t>(round_up(pl.n_tiles * 4, 256));
     const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
     if (counter_bytes + partial_bytes > static_cast<size_t>(GEMM_F16_NOALLOC_SCRATCH_BYTES))
@@ -660,7 +798,7 @@ gemm_status_t run_noalloc(const void* A, const void* B, void* D, int64_t M, int6
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    SkinnyParams p;
+    StreamKParams p;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
@@ -760,7 +898,7 @@ GEMM_API gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, gemm_va
     if (plan == nullptr) return GEMM_ERR_INVALID_VALUE;
     Limits lim;
     if (num_sms > 0) {
-        lim = Limits{num_sms, num_sms / 2, 1, 1};
+        lim = host_limits(num_sms);
     } else {
         DeviceState* dev = nullptr;
         const gemm_status_t st = get_device(&dev, nullptr);
@@ -775,7 +913,7 @@ GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N,
     if (plan == nullptr || !dtype_valid(dtype)) return GEMM_ERR_INVALID_VALUE;
     Limits lim;
     if (num_sms > 0) {
-        lim = Limits{num_sms, num_sms / 2, 1, 1};
+        lim = host_limits(num_sms);
     } else {
         DeviceState* dev = nullptr;
         const gemm_status_t st = get_device(&dev, nullptr);

@@ -205,14 +205,78 @@ inline int choose_ksplit(int64_t tiles, int64_t slots, int64_t k_blocks) {
     return s < 2 ? 1 : static_cast<int>(s);
 }
 
-// ------------------------------------------------------------------ skinny
-// Small-M kernel: D^T = B * A^T computed with the operands' roles swapped, so
-// the 128-row MMA side runs over N (the weight rows) and the narrow MMA N
-// side (MN = 16, 32 or 64) over M.  The (n-tile, k-block) units are split
-// into G contiguous ranges, one per CTA; tiles cut across ranges are summed
-// in a fixed order by the last CTA to finish one of their pieces.
+// ------------------------------------------------------------------ small M
+// Both small-M kernels compute D^T = B * A^T with the operands' roles
+// swapped, so the 128-row MMA side runs over N (the weight rows) and the
+// narrow MMA N side (MN = 16, 32 or 64) over M.
+//
+// Column-range kernel (the default).  N is cut into R ranges of `width` <= 128
+// consecutive columns (B rows).  A range belongs to one cluster of P CTAs;
+// CTA j of the cluster runs the j-th of P equal pieces of the K loop over the
+// range's B rows, and the P fp32 partials are summed inside the cluster
+// through distributed shared memory.  With P = 1 a CTA may own several
+// ranges (persistent, one after the other).
 template <int MN_>
 struct SkinnyConfig {
+    static constexpr int MN = MN_;
+    static constexpr int X_BYTES = MN * kStageRowBytes;    // activation (A) slot: MN rows
+    // A B slot holds the range's `width` rows; slots are width * 128 bytes
+    // rounded up to the 1024-byte swizzle atom, so narrow ranges pack more
+    // stages (bytes in flight) into the ring.  The MMA reads 128 rows from a
+    // slot's base: past a narrow slot it reads the next slot (or, for the last
+    // one, the A slots and buffers behind the ring, all inside this CTA's
+    // shared memory); those rows only feed TMEM lanes that are never used.
+    static constexpr int MAX_STAGES = 32;
+    // partials received from the cluster: [P][MN / P][128] fp32 = MN * 128 fp32
+    static constexpr int RECV_BYTES = MN * 128 * 4;
+    static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
+    static constexpr int TMEM_COLS = (2 * MN < 32) ? 32 : 2 * MN;
+    // ring = [stages B slots][stages A slots], split at run time (ring_stages)
+    static constexpr int RING_BYTES = (kMaxDynSmem - 1024 - RECV_BYTES - NUM_BARS * 8 - 16) / 1024 * 1024;
+    static constexpr int OFF_RECV = RING_BYTES;
+    static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
+    static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
+    static_assert(RING_BYTES / (128 * kStageRowBytes + X_BYTES) >= 4, "at least four full-width stages");
+    static_assert(RECV_BYTES + NUM_BARS * 8 >= 0, "layout");
+    static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
+    static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
+};
+
+// Stride of a B slot for ranges of `width` columns; a launch's ring has
+// min(MAX_STAGES, RING_BYTES / (stride + X_BYTES)) stages.
+GEMM_HD int skinny_w_stride(int width) { return (width * kStageRowBytes + 1023) / 1024 * 1024; }
+
+using CfgSkinny16 = SkinnyConfig<16>;
+using CfgSkinny32 = SkinnyConfig<32>;
+using CfgSkinny64 = SkinnyConfig<64>;
+
+// Largest cluster (K pieces per column range) of the column-range kernel.
+constexpr int kSkinnyMaxPieces = 8;
+
+struct SkinnyParams {
+    int32_t M, N, K;
+    int32_t k_blocks;
+    int32_t width;            // columns per range (rows of a B box), 1..128
+    int32_t ranges;           // R; range r covers columns [r * width, r * width + width) (clipped at N)
+    int32_t pieces;           // P = CTAs per cluster; CTA j runs K blocks [j kb / P, (j + 1) kb / P)
+    int32_t stages;           // ring stages, each a B slot of w_stride bytes and an A slot
+    int32_t w_stride;         // skinny_w_stride(width)
+    void* D;                  // fp16 or bf16 [M][N]
+    EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int32_t stream_b;         // B is too large to stay in L2: load it evict-first
+    uint32_t ab_format;       // operand format field of the MMA instruction descriptor
+};
+
+// Stream-K kernel (GEMM_VARIANT_SKINNY_STREAMK, and the no-allocation entry
+// point).  The (n-tile, k-block) units are split into G contiguous ranges,
+// one per CTA; tiles cut across ranges are summed in a fixed order, through a
+// global-memory workspace, by the last CTA to finish one of their pieces.
+template <int MN_>
+struct StreamKConfig {
     static constexpr int MN = MN_;
     static constexpr int W_BYTES = 128 * kStageRowBytes;   // weight (B) tile: 128 rows
     static constexpr int X_BYTES = MN * kStageRowBytes;    // activation (A) tile: MN rows
@@ -233,11 +297,11 @@ struct SkinnyConfig {
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
 };
 
-using CfgSkinny16 = SkinnyConfig<16>;
-using CfgSkinny32 = SkinnyConfig<32>;
-using CfgSkinny64 = SkinnyConfig<64>;
+using CfgStreamK16 = StreamKConfig<16>;
+using CfgStreamK32 = StreamKConfig<32>;
+using CfgStreamK64 = StreamKConfig<64>;
 
-struct SkinnyParams {
+struct StreamKParams {
     int32_t M, N, K;
     int32_t n_tiles, k_blocks;
     int32_t num_ctas;         // G
@@ -254,7 +318,7 @@ struct SkinnyParams {
 };
 
 // B of at least this many bytes is read once per call and cannot stay in the
-// 129 MB L2 until the next one, so the small-M kernel streams it with an
+// 129 MB L2 until the next one, so the small-M kernels stream it with an
 // evict-first policy (keeping A and the fp32 partials in L2 instead).
 constexpr int64_t kStreamBBytes = 96ll << 20;
 

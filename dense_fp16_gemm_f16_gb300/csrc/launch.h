@@ -25,9 +25,19 @@ struct TiledOps {
 };
 
 struct SkinnyOps {
+    // the ring a launch divides into min(max_stages, ring_bytes / (B slot + x_bytes)) stages
+    int mn, ring_bytes, x_bytes, max_stages, smem_bytes, tmem_cols;
+    cudaError_t (*prepare)();
+    // co-resident clusters of `pieces` CTAs on the current device
+    cudaError_t (*max_active)(int pieces, int* out);
+    cudaError_t (*launch)(const CUtensorMap& w, const CUtensorMap& x, const SkinnyParams& p,
+                          int grid_ctas, cudaStream_t stream);
+};
+
+struct StreamKOps {
     int mn, stages, smem_bytes, tmem_cols;
     cudaError_t (*prepare)();
-    cudaError_t (*launch)(const CUtensorMap& w, const CUtensorMap& x, const SkinnyParams& p,
+    cudaError_t (*launch)(const CUtensorMap& w, const CUtensorMap& x, const StreamKParams& p,
                           int grid_ctas, cudaStream_t stream);
 };
 
@@ -36,6 +46,7 @@ struct SkinnyOps {
 const TiledOps& tiled_ops_2cta256(int dtype);
 const TiledOps& tiled_ops_1cta128(int dtype);
 const TiledOps& tiled_ops_1cta256(int dtype);
-const SkinnyOps& skinny_ops(int mn, int dtype);  // mn = 16, 32 or 64
+const SkinnyOps& skinny_ops(int mn, int dtype);    // mn = 16, 32 or 64
+const StreamKOps& streamk_ops(int mn, int dtype);  // mn = 16, 32 or 64
 
 }  // namespace gemm_gb300

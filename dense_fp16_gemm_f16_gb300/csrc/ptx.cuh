@@ -86,6 +86,12 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// 32-bit store to shared memory given by its shared::cluster address (this or
+// a peer CTA of the cluster).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr_cluster, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr_cluster), "f"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
@@ -99,6 +105,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+
+// Prefetch a 2-D tile into L2 (nothing lands in shared memory, nothing is
+// waited for).  L2 is coherent, so a prefetch issued before the data's last
+// writer has finished can never make a later load see stale data.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(map), "r"(x), "r"(y) : "memory");
 }
 
 // L2 cache policies for the .L2::cache_hint forms below.
@@ -315,6 +329,17 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+// MN (16, 32 or 64) consecutive columns of this thread's TMEM lane.
+template <int MN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[MN]) {
+    if constexpr (MN == 16) {
+        tmem_ld_x16(taddr, v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < MN / 32; ++i) tmem_ld_x32(taddr + 32 * i, v + 32 * i);
+    }
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

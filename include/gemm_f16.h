@@ -26,12 +26,17 @@
  *   - Argument errors are returned synchronously and nothing is enqueued.
  *   - The library uses the CUDA device that is current on the calling thread.
  *
- * Scratch memory.  The split-K kernels (small-M, and 2-CTA tiles with a
- * split K loop) keep fp32 partial sums and per-tile counters in a workspace the library allocates with
- * cudaMalloc on the first call that needs it for a given (device, stream)
- * pair, grows when a larger problem needs more, and keeps until the process
- * exits.  Calls on the same stream are ordered and share that workspace
- * safely; calls on different streams get different workspaces.
+ * Scratch memory.  Two kernels keep fp32 partial sums and per-tile counters
+ * in global memory: the 2-CTA tiles with a split K loop
+ * (GEMM_VARIANT_TILE_2CTA_SPLITK) and the stream-K small-M kernel
+ * (GEMM_VARIANT_SKINNY_STREAMK; the default small-M kernel sums its partials
+ * on chip and needs none).  That workspace is allocated with cudaMalloc on
+ * the first call that needs it for a given (device, stream) pair, grows when
+ * a larger problem needs more, and is kept until the process exits: a caller
+ * that runs these variants on many short-lived streams keeps one workspace
+ * per stream (each as large as the largest problem it ran).  Calls on the
+ * same stream are ordered and share that workspace safely; calls on
+ * different streams get different workspaces.
  *
  * CUDA graphs.  A call may be recorded by stream capture (and the graph
  * replayed on new contents of the same buffers) once one uncaptured call of
@@ -79,11 +84,17 @@ typedef enum {
     GEMM_VARIANT_TILE_2CTA_256x256 = 1, /* persistent, 2-CTA cluster, 256x256 tile per pair */
     GEMM_VARIANT_TILE_1CTA_128x128 = 2, /* persistent, one CTA per 128x128 tile */
     GEMM_VARIANT_TILE_1CTA_128x256 = 3, /* persistent, one CTA per 128x256 tile */
-    GEMM_VARIANT_SKINNY_SPLITK = 4,     /* M <= 64: operands swapped, K split across all SMs */
+    GEMM_VARIANT_SKINNY_SPLITK = 4,     /* M <= 64: operands swapped; N in column ranges, each
+                                           range's K loop split over the CTAs of one cluster,
+                                           partials summed in distributed shared memory */
     GEMM_VARIANT_TILE_2CTA_SPLITK = 5   /* 2-CTA 256x256 tiles with each tile's K loop split over
                                            several CTA pairs (for shapes with few tiles); falls
                                            back to GEMM_VARIANT_TILE_2CTA_256x256 when the tiles
-                                           already fill the GPU */
+                                           already fill the GPU */,
+    GEMM_VARIANT_SKINNY_STREAMK = 6     /* M <= 64: operands swapped; (tile, K block) units dealt
+                                           in equal contiguous ranges to all SMs, split tiles
+                                           summed through the fp32 workspace (the kernel of
+                                           gemm_f16_nt_noalloc) */
 } gemm_variant_t;
 
 /* Element type of A and B; both operands share it and the MMA accumulates in
@@ -226,17 +237,21 @@ typedef struct {
     int32_t tile_n;          /* output columns per tile */
     int32_t tile_k;          /* K elements per pipeline stage */
     int32_t stages;          /* shared-memory pipeline depth */
-    int64_t m_tiles, n_tiles;/* tile grid (skinny: m_tiles = 1, n_tiles = N tiles of 128) */
+    int64_t m_tiles, n_tiles;/* tile grid (small M: m_tiles = 1; n_tiles = column ranges of
+                                tile_n columns, or tiles of 128 for the stream-K kernel) */
     int64_t k_blocks;        /* ceil(K / tile_k) */
     int32_t grid_ctas;       /* CTAs launched */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t tmem_cols;       /* TMEM columns allocated per CTA */
-    int32_t max_tiles_per_cta; /* skinny: partial-sum slots per CTA, else 0 */
-    int64_t workspace_bytes; /* skinny: fp32 partials + counters, else 0 */
+    int32_t max_tiles_per_cta; /* small M: column ranges per CTA (stream-K: partial-sum
+                                  slots per CTA), else 0 */
+    int64_t workspace_bytes; /* fp32 partials + counters of the stream-K and tiled
+                                split-K kernels, else 0 */
     int64_t num_full_tiles;  /* tiled: tiles run whole (the persistent grid's full rounds) */
     int32_t tail_split;      /* tiled: the other tiles are cut into this many column pieces */
     int32_t group_m;         /* tiled: tile rows per raster group (L2 reuse of A) */
-    int32_t k_split;         /* tiled split-K: pieces per tile's K loop (1 = none) */
+    int32_t k_split;         /* pieces per tile's K loop (1 = none): tiled split-K, or the
+                                CTAs per cluster of the column-range small-M kernel */
     int32_t reserved;
 } gemm_plan_t;
 
@@ -274,8 +289,10 @@ GEMM_API gemm_status_t gemm_nt_plan_ex(gemm_dtype_t dtype, int64_t M, int64_t N,
  * 16 MiB), which every GPU that loads the library holds until the process exits.
  *
  * Arguments, layout, ownership and semantics are those of gemm_f16_nt; the
- * caller still passes A, B and D (device memory).  It runs the same split-K
- * kernel as GEMM_VARIANT_SKINNY_SPLITK and gives the same D.
+ * caller still passes A, B and D (device memory).  It runs the stream-K
+ * kernel of GEMM_VARIANT_SKINNY_STREAMK on the array and gives the same D as
+ * that variant (bitwise); against gemm_f16_nt, which runs the column-range
+ * small-M kernel, D agrees up to the order of the fp32 additions.
  *
  * Errors: those of gemm_f16_nt, plus GEMM_ERR_INVALID_VALUE when M > 64 or when
  * the problem needs more scratch than the fixed array holds (nothing is then

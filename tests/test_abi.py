@@ -66,6 +66,7 @@ def test_argument_errors_are_returned_before_any_device_call(lib):
     assert _call(2 ** 31, 8, 8) == S.ERR_INVALID_VALUE
     assert _call(8, 8, 8, variant=7) == S.ERR_INVALID_VALUE
     assert _call(65, 8, 8, variant=g.Variant.SKINNY_SPLITK) == S.ERR_INVALID_VALUE
+    assert _call(65, 8, 8, variant=g.Variant.SKINNY_STREAMK) == S.ERR_INVALID_VALUE
     # empty problems are a no-op even with NULL pointers
     assert _call(0, 8, 8, A=0, B=0, D=0) == S.OK
     assert _call(8, 0, 8, A=0, B=0, D=0) == S.OK
@@ -188,9 +189,16 @@ def test_plans_for_the_named_workloads(lib):
     assert p["variant"] == "TILE_1CTA_128x128" and p["k_blocks"] == 1
     assert (p["tail_split"], p["grid_ctas"]) == (2, 2)
     p = P(16, 8192, 8192)
-    assert p["variant"] == "SKINNY_SPLITK" and p["tile_m"] == 16 and p["n_tiles"] == 64
-    assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 2
-    assert p["workspace_bytes"] >= 152 * 2 * 16 * 128 * 4 + 64 * 4
+    # 76 column ranges of 108 columns, each range's K loop in 2 pieces (a
+    # cluster of 2 CTAs): all 152 SMs, no workspace
+    assert p["variant"] == "SKINNY_SPLITK" and p["tile_m"] == 16
+    assert (p["n_tiles"], p["tile_n"], p["k_split"]) == (76, 108, 2)
+    assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 1 and p["workspace_bytes"] == 0
+    # the stream-K kernel on request: 64 tiles of 128 columns dealt over 152 CTAs
+    q = P(16, 8192, 8192, variant=g.Variant.SKINNY_STREAMK)
+    assert q["variant"] == "SKINNY_STREAMK" and q["n_tiles"] == 64
+    assert q["grid_ctas"] == 152 and q["max_tiles_per_cta"] == 2
+    assert q["workspace_bytes"] >= 152 * 2 * 16 * 128 * 4 + 64 * 4
     for v in g.Variant:
         if v in (g.Variant.AUTO,):
             continue
@@ -199,15 +207,32 @@ def test_plans_for_the_named_workloads(lib):
         assert q["smem_bytes"] <= 232448
 
 
-def test_skinny_split_covers_every_unit_once(lib):
-    # tiny problems: fewer (tile, k-block) units than SMs -> one unit per CTA
-    p = g.gemm_f16_nt_plan(5, 8, 8, num_sms=152)
-    assert p["variant"] == "SKINNY_SPLITK" and p["grid_ctas"] == 1 and p["tile_m"] == 16
-    p = g.gemm_f16_nt_plan(33, 1024, 640, num_sms=152)
-    assert p["tile_m"] == 64 and p["grid_ctas"] == 8 * 10
-    # many tiles with short K: each CTA owns several whole tiles
-    p = g.gemm_f16_nt_plan(16, 65536, 64, num_sms=152)
-    assert p["grid_ctas"] == 152 and p["max_tiles_per_cta"] == 4   # 512 whole tiles over 152 CTAs
+def test_skinny_ranges_and_pieces(lib):
+    P = lambda *a, **k: g.gemm_f16_nt_plan(*a, num_sms=152, **k)  # noqa: E731
+    # one K block: no split; one range per column
+    p = P(5, 8, 8)
+    assert p["variant"] == "SKINNY_SPLITK" and p["tile_m"] == 16
+    assert (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (1, 8, 1, 8)
+    # short K, few columns: 19 ranges of 54 columns in clusters of 8 (152 ranges of
+    # 7 columns would leave the ring mostly empty: too few bytes in flight)
+    p = P(33, 1024, 640)
+    assert p["tile_m"] == 64 and (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (8, 19, 54, 152)
+    # very short K: every CTA one range of 14 columns, no split
+    p = P(7, 2048, 192)
+    assert (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (1, 152, 14, 152)
+    assert p["stages"] == 32     # narrow B slots: the ring holds its most stages
+    # few columns, long K: clusters of 8 pieces, 19 ranges of 54 columns
+    p = P(16, 1024, 8192)
+    assert (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (8, 19, 54, 152)
+    # many columns, short K: every CTA owns 4 ranges of 108 columns in turn
+    p = P(16, 65536, 64)
+    assert (p["k_split"], p["grid_ctas"], p["max_tiles_per_cta"], p["n_tiles"], p["tile_n"]) == (1, 152, 4, 608, 108)
+    # ranges never exceed 128 columns, and the split never exceeds the K blocks
+    for (M, N, K) in [(1, 8, 64), (64, 16384, 2048), (16, 19456, 8192), (16, 19464, 8192), (7, 2048, 192)]:
+        p = P(M, N, K)
+        assert p["tile_n"] <= 128 and p["n_tiles"] * p["tile_n"] >= N
+        assert p["k_split"] <= p["k_blocks"] and p["grid_ctas"] <= 152
+        assert p["grid_ctas"] == (p["n_tiles"] * p["k_split"] if p["k_split"] > 1 else min(p["n_tiles"], 152))
 
 
 def test_tail_split_minimises_the_last_round(lib):
@@ -260,7 +285,7 @@ def test_plans_for_8bit_operands(lib):
     with pytest.raises(g.GemmError):
         P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units
     p = P(16, 8192, 8192)
-    assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and p["max_tiles_per_cta"] == 2
+    assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and (p["k_split"], p["n_tiles"]) == (2, 76)
     p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: a split by 4
     assert p["variant"] == "TILE_2CTA_256x256" and p["k_split"] == 1     # would save only 48: unsplit pairs
     p = P(512, 1024, 16384)                                  # 128 K blocks over 8 pieces: split
@@ -289,6 +314,8 @@ def test_plan_errors(lib):
         g.gemm_f16_nt_plan(-1, 8, 8, num_sms=152)
     with pytest.raises(g.GemmError):
         g.gemm_f16_nt_plan(100, 8, 8, variant=g.Variant.SKINNY_SPLITK, num_sms=152)
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_nt_plan(100, 8, 8, variant=g.Variant.SKINNY_STREAMK, num_sms=152)
     with pytest.raises(g.GemmError):
         g.gemm_f16_nt_plan(8, 8, 9, num_sms=152)
 

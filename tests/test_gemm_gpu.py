@@ -106,11 +106,37 @@ def test_tiled_variants_ragged(variant, shape):
     _full_parity(A, B, variant)
 
 
+@pytest.mark.parametrize("variant", [g.Variant.SKINNY_SPLITK, g.Variant.SKINNY_STREAMK], ids=lambda v: v.name)
 @pytest.mark.parametrize("shape", SKINNY, ids=lambda s: "x".join(map(str, s)))
-def test_skinny_variant_ragged(shape):
+def test_skinny_variant_ragged(shape, variant):
     M, N, K = shape
     A, B = inputs.operands(M, N, K, "normal:1", "normal:1/sqrtK", seed=2000 + M + N + K)
+    _full_parity(A, B, variant)
+
+
+# shapes the column-range small-M planner gives 8, 4, 2 and 1 K pieces per
+# range (clusters of that many CTAs), and one whose ranges take two rounds
+SKINNY_CLUSTERS = [(16, 1024, 8192), (16, 2560, 8192), (24, 3000, 4104), (16, 8192, 4096), (33, 1000, 520),
+                   (8, 24576, 256), (64, 1032, 1032), (40, 4096, 2048), (1, 8, 8192), (7, 2048, 192),
+                   (1, 8192, 1024)]
+
+
+def test_skinny_cluster_sizes_all_covered():
+    plans = [g.gemm_f16_nt_plan(*s) for s in SKINNY_CLUSTERS]
+    assert {p["k_split"] for p in plans} == {1, 2, 4, 8}, [(p["k_split"], p["n_tiles"]) for p in plans]
+    assert any(p["max_tiles_per_cta"] > 1 for p in plans)
+    assert all(p["variant"] == "SKINNY_SPLITK" and p["tile_n"] <= 128 for p in plans)
+
+
+@pytest.mark.parametrize("shape", SKINNY_CLUSTERS, ids=lambda s: "x".join(map(str, s)))
+def test_skinny_cluster_sizes(shape):
+    # full output against the oracle, and the same bits on a second call
+    M, N, K = shape
+    A, B = inputs.operands(M, N, K, "normal:1", "normal:1/sqrtK", seed=2500 + M + N + K)
     _full_parity(A, B, g.Variant.SKINNY_SPLITK)
+    d1 = _run(A, B, g.Variant.SKINNY_SPLITK)
+    d2 = _run(A, B, g.Variant.SKINNY_SPLITK)
+    assert np.array_equal(d1.view(np.uint16), d2.view(np.uint16))
 
 
 @pytest.mark.parametrize("shape", [(300, 520, 1000), (513, 256, 4104), (1000, 1000, 640), (1024, 1024, 2048),
@@ -142,9 +168,11 @@ def test_all_variants_agree(shape):
 
 
 # ---------------------------------------------------------------- closed forms (exact)
-@pytest.mark.parametrize("variant", TILED + [g.Variant.SKINNY_SPLITK], ids=lambda v: v.name)
+@pytest.mark.parametrize("variant", TILED + [g.Variant.SKINNY_SPLITK, g.Variant.SKINNY_STREAMK],
+                         ids=lambda v: v.name)
 def test_closed_forms_exact(variant):
-    M = 48 if variant == g.Variant.SKINNY_SPLITK else 272
+    skinny = variant in (g.Variant.SKINNY_SPLITK, g.Variant.SKINNY_STREAMK)
+    M = 48 if skinny else 272
     # all ones: D = K exactly (fp32 holds every partial sum exactly)
     for K in (64, 4104):
         d = _run(np.ones((M, K), np.float16), np.ones((264, K), np.float16), variant)
@@ -156,7 +184,7 @@ def test_closed_forms_exact(variant):
     assert np.array_equal(d.view(np.uint16), A.view(np.uint16))
     # swapping the operands transposes D
     B = inputs.draw(136, K, "uniform", seed=6)
-    if variant == g.Variant.SKINNY_SPLITK:
+    if skinny:
         return
     d1 = _run(A, B, variant)
     d2 = _run(B, A, variant)
@@ -188,12 +216,13 @@ def test_bitwise_deterministic(name_or_shape):
     assert np.array_equal(d1.view(np.uint16), d2.view(np.uint16))
 
 
-def test_skinny_split_tiles_rearm_between_calls():
-    # every tile's K loop is split over many CTAs: the fixed-order reduction
-    # and the counter reset are exercised on consecutive calls
+@pytest.mark.parametrize("variant", [g.Variant.SKINNY_SPLITK, g.Variant.SKINNY_STREAMK], ids=lambda v: v.name)
+def test_skinny_split_tiles_rearm_between_calls(variant):
+    # every tile's K loop is split over several CTAs: the fixed-order reduction
+    # (and, for the stream-K kernel, the counter reset) on consecutive calls
     for seed in (1, 2, 3):
         A, B = inputs.operands(16, 1024, 8192, "normal:1", "normal:1/sqrtK", seed=seed)
-        _full_parity(A, B, g.Variant.SKINNY_SPLITK, what=f"skinny split seed {seed}")
+        _full_parity(A, B, variant, what=f"{variant.name} seed {seed}")
 
 
 def test_side_stream():

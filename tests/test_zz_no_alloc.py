@@ -12,7 +12,9 @@ finds the array as the first one left it):
     with NaN so an unwritten element fails, within the tolerance the other
     parity tests use;
   - the output against the existing entry point gemm_f16_nt on the same
-    operands, within the same tolerance;
+    operands, within the same tolerance (gemm_f16_nt runs the column-range
+    small-M kernel, the no-allocation entry the stream-K one, so the two
+    paths share no kernel);
   - a problem near the array's size limit (M = 64, N = 16384: two partial-sum
     slots per CTA), and that a problem too large for the array is refused.
 It sits in a file of its own, named so that pytest collects it last.
@@ -61,7 +63,7 @@ def test_noalloc_matches_oracle_and_gemm_f16_nt_on_two_calls_in_a_row(lib, shape
     M, N, K = shape
     if (M, N) == (64, 16384):
         # near the limit: two partial-sum slots per CTA fill most of the array
-        plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.SKINNY_SPLITK)
+        plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.SKINNY_STREAMK)
         assert plan["max_tiles_per_cta"] == 2
         assert plan["workspace_bytes"] <= 16 << 20
     for call in (1, 2):
