@@ -56,6 +56,7 @@ struct DeviceState {
     int per_sm_1cta128 = 0;      // co-resident CTAs per SM
     int per_sm_1cta256 = 0;
     int skinny_clusters[kSkinnyMaxPieces + 1] = {};   // co-resident small-M clusters of P CTAs
+    int split_clusters[kSplitMaxPieces + 1] = {};     // co-resident split-K clusters of S CTA pairs
 };
 
 struct Workspace {
@@ -80,16 +81,17 @@ constexpr int64_t kMaxDim = INT32_MAX;
 // 4000 x 11000 x 4104.  GEMM_GROUP_M fixes the group size instead.
 constexpr int64_t kL2GroupBytes = 48ll << 20;
 // AUTO's choice for shapes whose 256x256 tiles fill less than one round of CTA
-// pairs, from launches timed back to back on GB300 (fp16 and E4M3 alike, in
-// K blocks of one 128-byte stage each):
-//   unsplit, one tile per pair:   ~3 us + 0.25 us per K block
-//   split into S pieces:         ~14 us + 0.25 us per K block of a piece
-// (publishing and re-reading the fp32 partials is the difference), so a split
-// pays when kb * (1 - 1/S) reaches ~56 blocks.  Measured: fp16 512x2048x8192
-// (kb 128, S 4) 23.9 us split / 32.5 unsplit; fp16 1024x2048x5120 (kb 80, S 2)
-// 26.0 / 23.3; E4M3 512x2048x8192 (kb 64, S 4) 20.9 / 19.3; E4M3 768x2048x6144
-// (kb 48, S 3) 23.0 / 16.7; E4M3 512x1024x16384 (kb 128, S 8) 19.1 / 32.7.
-constexpr int64_t kSplitKSavedBlocks = 56;
+// pairs: split each tile's K loop over a cluster of S pairs when the K blocks
+// a split saves, kb * (1 - 1/S), reach kSplitKSavedBlocks.  A K block (one
+// 128-byte stage) takes a pair ~0.25 us; in back-to-back launches on GB300 a
+// split launch costs ~10 us more than an unsplit one (exchanging the fp32
+// partials through distributed shared memory ~3 us, the cluster barriers
+// ~2 us, the slice sums and D stores ~2 us, a slower ramp and teardown).
+// Measured (fp16, us, split / unsplit pairs / 128x256 CTAs): 512x2048x8192 S=3
+// 23.8 / 32.5 / 35.3; 768x2048x6144 S=2 24.5 / 26.5 / 29.0; 1024x2048x5120 S=2
+// 23.1 / 23.4 / 25.1; 1024x1024x4096 S=3 18.0 / 19.0 / 19.7; 1024x1024x2048
+// S=3 14.7 / 12.2 / 11.9; 256x256x8192 S=4 19.1 / 32.0 / 34.7.
+constexpr int64_t kSplitKSavedBlocks = 40;
 // Unsplit, the pair kernel beats 128x256 tiles on single CTAs once the K loop
 // is long enough for its halved operand traffic per FLOP to matter (fp16
 // 1024x2048x5120: 23.3 against 25.2 us; E4M3 512x2048x8192: 19.3 against
@@ -145,12 +147,14 @@ struct Limits {
     int per_sm_1cta128;
     int per_sm_1cta256;
     int skinny_clusters[kSkinnyMaxPieces + 1];   // index P: co-resident clusters of P CTAs (0: unknown)
+    int split_clusters[kSplitMaxPieces + 1];     // index S: co-resident clusters of S CTA pairs
 };
 
 // A pure-host planner's view of a GPU with `sms` SMs (nothing queried).
 Limits host_limits(int sms) {
-    Limits lim{sms, sms / 2, 1, 1, {}};
+    Limits lim{sms, sms / 2, 1, 1, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; pc *= 2) lim.skinny_clusters[pc] = sms / pc;
+    for (int s = 1; s <= kSplitMaxPieces; ++s) lim.split_clusters[s] = sms / (2 * s);
     return lim;
 }
 
@@ -255,7 +259,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             // and short ones to single CTAs (kPairMinBlocks).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
             const int64_t kb = cdiv(K, bk);
-            const int ks = choose_ksplit(t2, pairs, kb);
+            const int ks = choose_ksplit(t2, lim.split_clusters, kb);
             if (t2 >= pairs && kb <= (in_bytes == 1 ? kShortKBlocks8 : kShortKBlocks16))
                 variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else if (t2 >= pairs)
@@ -322,8 +326,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     }
 
     if (variant == GEMM_VARIANT_TILE_2CTA_SPLITK &&
-        choose_ksplit(cdiv(M, 256) * cdiv(N, 256), pairs, pl->k_blocks) < 2)
-        variant = GEMM_VARIANT_TILE_2CTA_256x256;   // enough tiles already: no split
+        choose_ksplit(cdiv(M, 256) * cdiv(N, 256), lim.split_clusters, pl->k_blocks) < 2)
+        variant = GEMM_VARIANT_TILE_2CTA_256x256;   // too many tiles for one wave of clusters: no split
     pl->variant = variant;
     const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK;
     const TiledOps& ops = tiled_ops_of(variant, 0);
@@ -349,18 +353,21 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     int64_t num_full;
     int split;
     int ksplit = 1;
+    int64_t clusters;
     if (ksplit_variant) {
-        ksplit = choose_ksplit(tiles, slots, pl->k_blocks);
+        // one cluster of ksplit pairs per tile, all resident in one wave
+        ksplit = choose_ksplit(tiles, lim.split_clusters, pl->k_blocks);
         num_full = tiles;
         split = 1;
-        pl->workspace_bytes = round_up(tiles * ksplit * ops.tile_m * ops.tile_n * 4, 256) + round_up(tiles * 4, 256);
+        clusters = tiles;
+        pl->grid_ctas = static_cast<int32_t>(tiles * ksplit * ops.cluster);
     } else {
         tail_split(tiles, slots, ops.tile_n, ops.cta_group, num_full, split);
+        const int64_t units = num_full + (tiles - num_full) * split;
+        clusters = units < slots ? units : slots;
+        pl->grid_ctas = static_cast<int32_t>(clusters * ops.cluster);
     }
     pl->k_split = ksplit;
-    const int64_t units = ksplit > 1 ? tiles * ksplit : num_full + (tiles - num_full) * split;
-    const int64_t clusters = units < slots ? units : slots;
-    pl->grid_ctas = static_cast<int32_t>(clusters * ops.cluster);
     pl->num_full_tiles = num_full;
     pl->tail_split = split;
     pl->group_m = static_cast<int32_t>(raster_group(pl->m_tiles, ops.tile_m, K, in_bytes));
@@ -427,11 +434,20 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
         d.max_clusters_2cta = clusters;
         d.per_sm_1cta128 = per128;
         d.per_sm_1cta256 = per256;
+        // co-resident clusters of each size the planner may use (a size the
+        // device cannot run at all counts as zero: the planner avoids it)
         d.skinny_clusters[1] = sms;
         for (int pc = 2; pc <= kSkinnyMaxPieces; pc *= 2) {
             if (skinny_ops(16, 0).max_active(pc, &d.skinny_clusters[pc]) != cudaSuccess) {
                 cudaGetLastError();
-                return GEMM_ERR_CUDA;
+                d.skinny_clusters[pc] = 0;
+            }
+        }
+        d.split_clusters[1] = clusters;
+        for (int sp = 2; sp <= kSplitMaxPieces; ++sp) {
+            if (tiled[0]->max_active_split(sp, &d.split_clusters[sp]) != cudaSuccess) {
+                cudaGetLastError();
+                d.split_clusters[sp] = 0;
             }
         }
         d.ready = true;
@@ -442,8 +458,9 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    Limits lim{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256, {}};
+    Limits lim{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; ++pc) lim.skinny_clusters[pc] = d.skinny_clusters[pc];
+    for (int sp = 1; sp <= kSplitMaxPieces; ++sp) lim.split_clusters[sp] = d.split_clusters[sp];
     return lim;
 }
 
@@ -681,13 +698,6 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     }
 
     const TiledOps& ops = tiled_ops_of(static_cast<gemm_variant_t>(pl.variant), dtype);
-    Workspace* ws = nullptr;
-    if (pl.k_split > 1) {
-        const size_t partial_bytes = static_cast<size_t>(pl.m_tiles * pl.n_tiles) * pl.k_split * ops.tile_m *
-                                     ops.tile_n * sizeof(float);
-        st = get_workspace(dev_id, stream, partial_bytes, static_cast<size_t>(pl.m_tiles * pl.n_tiles), &ws);
-        if (st != GEMM_OK) return st;
-    }
     CUtensorMap ta, tb, tbp, td;
     const uint32_t b_rows = static_cast<uint32_t>(ops.b_box_rows);
     if (!encode_2d(&ta, A, K, M, bk, 128, dtype) || !encode_2d(&tb, B, K, N, bk, b_rows, dtype) ||
@@ -708,10 +718,8 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.ksplit = pl.k_split;
     p.ab_format = dtype_ab_format(dtype);
     p.last_k_steps = static_cast<int32_t>(cdiv(K * in_bytes - (pl.k_blocks - 1) * kStageRowBytes, 32));
-    p.num_units = pl.k_split > 1 ? p.num_tiles * pl.k_split
+    p.num_units = pl.k_split > 1 ? p.num_tiles
                                  : pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
-    p.partials = ws ? ws->partials : nullptr;
-    p.counters = ws ? ws->counters : nullptr;
     p.D = D;
     p.epi = epi;
     p.status = dev->status;

@@ -103,13 +103,12 @@ struct TiledParams {
     int64_t num_full;         // tiles run whole: the persistent grid's full rounds
     int64_t num_units;        // num_full + (num_tiles - num_full) * split
     int32_t split;            // the remaining tiles are cut into `split` column pieces
-    int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces (split-K)
+    int32_t ksplit;           // > 1: every tile's K loop is cut into ksplit pieces, run by the
+                              // ksplit MMA groups of one cluster (split K)
     uint32_t ab_format;       // operand format field of the MMA instruction descriptor
     int32_t last_k_steps;     // 32-byte K steps of real data in the last K block (1..4)
-    float* partials;          // split-K: [num_tiles][ksplit][BM][BN] fp32
-    uint32_t* counters;       // split-K: [num_tiles], zero between calls
     void* D;                  // the output (fp16 or bf16 [M][N]); written directly by the
-                              // split-K slice reductions, through tmD otherwise
+                              // split-K slice sums, through tmD otherwise
     EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
     uint32_t* status;         // device status word (0 = ok)
     uint64_t timeout_ns;      // per-wait budget
@@ -136,17 +135,18 @@ GEMM_HD int ring_stride(const TiledParams& p, int a_bytes, int b_bytes) {
 }
 
 // Work unit u of the persistent loop -> (tile row tm, first column n0,
-// column count nw).  The first num_full units are whole tiles in raster
-// order; the tiles of the last, partly filled round are cut into `split`
-// column pieces so that more CTA pairs share that round.
-GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int64_t& tm, int64_t& n0, int& nw,
+// column count nw, K blocks [kb0, kb1)).  The first num_full units are whole
+// tiles in raster order; the tiles of the last, partly filled round are cut
+// into `split` column pieces so that more CTA pairs share that round.  With
+// split K, unit u is tile u and MMA group `group` of the cluster runs the
+// group-th of ksplit even shares of its K blocks.
+GEMM_HD void work_unit(int64_t u, const TiledParams& p, int BN, int group, int64_t& tm, int64_t& n0, int& nw,
                        int& kb0, int& kb1) {
     kb0 = 0;
     kb1 = p.k_blocks;
     if (p.ksplit > 1) {
-        // split-K: unit u is piece j of tile t; the pieces split the K blocks evenly
-        const int64_t t = div_nonneg(u, p.ksplit);
-        const int j = static_cast<int>(u - t * p.ksplit);
+        const int64_t t = u;
+        const int j = group;
         int64_t tn;
         tile_coords(t, p.m_tiles, p.n_tiles, p.group_m, tm, tn);
         nw = BN;
@@ -194,15 +194,21 @@ inline void tail_split(int64_t num_tiles, int64_t slots, int BN, int CG, int64_t
     }
 }
 
-// Split-K factor for the pair kernel when its tiles do not fill a round of
-// CTA pairs: as many pieces per tile as keep every unit resident at once
-// (tiles * S <= slots), at most 8, and at least 4 K blocks per piece.
-inline int choose_ksplit(int64_t tiles, int64_t slots, int64_t k_blocks) {
-    if (tiles <= 0 || tiles * 2 > slots) return 1;
-    int64_t s = slots / tiles;
-    if (s > 8) s = 8;
-    if (s > k_blocks / 4) s = k_blocks / 4;
-    return s < 2 ? 1 : static_cast<int>(s);
+// Split-K factor for the pair kernel (clusters of S pairs, S <= 4 so that a
+// cluster has at most the 8 CTAs every GPU of this class supports): the most
+// pieces such that every tile's cluster is resident in one wave
+// (tiles <= clusters[S], the co-resident clusters of S pairs) and every piece
+// keeps at least kSplitMinBlocks K blocks; 1 = no split.
+constexpr int kSplitMaxPieces = 4;
+constexpr int64_t kSplitMinBlocks = 4;
+inline int choose_ksplit(int64_t tiles, const int* clusters, int64_t k_blocks) {
+#ifdef GEMM_SPLIT_PIECES
+    // a build that fixes S (waves of clusters allowed), for measurements
+    if (tiles > 0 && k_blocks >= kSplitMinBlocks * GEMM_SPLIT_PIECES) return GEMM_SPLIT_PIECES;
+#endif
+    for (int s = kSplitMaxPieces; s >= 2; --s)
+        if (tiles > 0 && tiles <= clusters[s] && k_blocks >= kSplitMinBlocks * s) return s;
+    return 1;
 }
 
 // ------------------------------------------------------------------ small M

@@ -41,156 +41,103 @@
 
 namespace gemm_gb300 {
 
-// Split-K partials of one piece are stored in a blocked column-major layout,
-// [BN/4 column quads][BM rows][4 columns] fp32: a thread (one row) moves four
-// consecutive columns with one 16-byte access, and the 32 lanes of a warp
-// (32 consecutive rows) cover one contiguous 512-byte run.
-template <int BM>
-__device__ __forceinline__ int64_t split_quad_offset(int col, int row) {
-    return (static_cast<int64_t>(col >> 2) * BM + row) * 4;
+// ---------------------------------------------------------------- split K
+// With p.ksplit = S > 1 a cluster of S * CG CTAs works on one tile: MMA group
+// j (a CTA pair, or one CTA) runs the j-th of S pieces of the tile's K loop,
+// and the S fp32 partials are summed in distributed shared memory.  Group j
+// finishes the j-th slice of the tile's columns (the BN / 8 groups of 8
+// columns dealt out evenly), for the rows its CTAs hold: every CTA stores
+// each column's partial into the receive buffer of the CTA of the same rank
+// in the group that finishes it, the cluster meets at a barrier, and each CTA
+// adds the S partials of its slice in ascending piece order -- a fixed order,
+// so the result does not depend on timing -- then applies the fused transform
+// and writes D.  The receive buffer takes the operand ring's space (the ring
+// is idle once every MMA of the cluster has finished, which the first of two
+// cluster barriers establishes).  No CTA waits on another cluster, so the
+// clusters need not be resident together.
+
+// First 8-column group of column slice j of a tile of kGroups groups.
+__device__ __forceinline__ int split_group_begin(int j, int k_groups, int S) { return j * k_groups / S; }
+// The slice that holds 8-column group g.
+__device__ __forceinline__ int split_slice_of(int g, int k_groups, int S) { return ((g + 1) * S - 1) / k_groups; }
+
+// Receive buffer layout: [S pieces][slice_quads][128 rows][4] fp32, where
+// slice_quads = 2 * ceil(k_groups / S) column quads: a thread (one row) moves
+// four consecutive columns with one 16-byte access, and consecutive rows are
+// consecutive 16-byte words (no bank conflicts on either side).
+__device__ __forceinline__ uint32_t split_recv_offset(int piece, int quad, int row, int slice_quads) {
+    return static_cast<uint32_t>(((piece * slice_quads + quad) * 128 + row) * 16);
 }
 
-// Sum of the S pieces of this thread's row over columns [c_begin, c_end) (a
-// multiple of 8 wide), pieces in ascending order, written to D (16-bit).
-// Loads go out in batches of up to 8 float4 (two 8-column groups when S = 2,
-// else one group with up to 4 pieces) before the additions that use them.
-template <class Cfg, class T, int S>
-__device__ __forceinline__ void split_k_reduce_row(const float* base, int r_local, int c_begin, int c_end,
-                                                   int64_t n0, int64_t grow, const TiledParams& p) {
-    constexpr int GB = (S <= 2) ? 2 : 1;            // 8-column groups per batch
-    constexpr int JC = (S < 4) ? S : 4;             // pieces per batch
-    const int64_t piece_stride = static_cast<int64_t>(Cfg::BM) * Cfg::BN;
-    T* D = static_cast<T*>(p.D);
+// Exchange: this CTA (group `piece`, pair rank `rank`) sends every 8-column
+// group of its partial (TMEM lane = row) to the CTA of the same rank in the
+// group that finishes the group's slice.  `ready` = the accumulator is valid
+// (else zeros are sent, so every receiver still gets every word it waits for).
+template <class Cfg>
+__device__ __forceinline__ void split_k_send(uint32_t recv_base, uint32_t t_row, bool ready, int piece, uint32_t rank,
+                                             int row, int S) {
+    constexpr int kGroups = Cfg::BN / 8;
+    const int slice_quads = 2 * ((kGroups + S - 1) / S);
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 8 * GB) {
-        float acc[GB][8];
-        uint4 cv[GB];   // C values, in flight with the partials
-#pragma unroll
-        for (int g = 0; g < GB; ++g) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = 0.0f;
-            const int64_t gcol = n0 + c + 8 * g;
-            cv[g] = (p.epi.on && c + 8 * g < c_end && gcol < p.N) ? epi_load_c8<T>(p.epi, grow, gcol, p.M, p.N)
-                                                                 : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j0 = 0; j0 < S; j0 += JC) {
-            float4 pv[GB][JC][2];
-#pragma unroll
-            for (int g = 0; g < GB; ++g) {
-                const int cg = c + 8 * g;
-#pragma unroll
-                for (int jj = 0; jj < JC; ++jj) {
-                    if (j0 + jj < S && cg < c_end) {
-                        const float* src = base + (j0 + jj) * piece_stride;
-                        pv[g][jj][0] = __ldcg(reinterpret_cast<const float4*>(src + split_quad_offset<Cfg::BM>(cg, r_local)));
-                        pv[g][jj][1] = __ldcg(reinterpret_cast<const float4*>(src + split_quad_offset<Cfg::BM>(cg + 4, r_local)));
-                    }
-                }
-            }
-#pragma unroll
-            for (int g = 0; g < GB; ++g) {
-#pragma unroll
-                for (int jj = 0; jj < JC; ++jj) {
-                    if (j0 + jj < S && c + 8 * g < c_end) {
-                        acc[g][0] += pv[g][jj][0].x; acc[g][1] += pv[g][jj][0].y;
-                        acc[g][2] += pv[g][jj][0].z; acc[g][3] += pv[g][jj][0].w;
-                        acc[g][4] += pv[g][jj][1].x; acc[g][5] += pv[g][jj][1].y;
-                        acc[g][6] += pv[g][jj][1].z; acc[g][7] += pv[g][jj][1].w;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < GB; ++g) {
-            const int cg = c + 8 * g;
-            const int64_t gcol = n0 + cg;
-            if (cg < c_end && gcol < p.N) {         // N % 8 == 0: groups are all in or all out
-                if (p.epi.on) epi_apply8_c<T>(p.epi, acc[g], cv[g], gcol);
-                uint32_t h[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(acc[g][2 * e], acc[g][2 * e + 1]);
-                *reinterpret_cast<uint4*>(D + grow * static_cast<int64_t>(p.N) + gcol) =
-                    make_uint4(h[0], h[1], h[2], h[3]);
-            }
-        }
-    }
-}
-
-// Split-K epilogue of one unit (piece j of tile t), run by the four epilogue
-// warps of each CTA of the pair: publish this piece's fp32 partial (this CTA's
-// 128 rows), wait until every piece of the tile is in, then sum all pieces of
-// this CTA's rows over the unit's 1/ksplit slice of columns -- pieces in
-// ascending order, so the result does not depend on timing -- and store that
-// slice of D.  The last CTA through re-arms the tile's counter.
-template <class Cfg, class T>
-__device__ __forceinline__ bool split_k_epilogue(const TiledParams& p, int64_t u, int64_t tm, int64_t n0,
-                                                 uint32_t t_row, uint32_t tempty_leader0, uint32_t tempty_local,
-                                                 uint32_t buf, int q, int lane, int etid, uint32_t rank) {
-    constexpr int CG = Cfg::CG;
-    constexpr int BN = Cfg::BN;
-    const int S = p.ksplit;
-    const int64_t t = u / S;
-    const int j = static_cast<int>(u - t * S);
-    const int r_local = static_cast<int>(rank) * 128 + q * 32 + lane;     // row within the pair's tile
-    // 1. partial of this piece: TMEM -> registers -> workspace
-    float* piece = p.partials + (t * S + j) * static_cast<int64_t>(BN) * Cfg::BM;
-#pragma unroll 1
-    for (int c = 0; c < BN / 64; ++c) {
+    for (int c = 0; c < Cfg::BN / 64; ++c) {
         uint32_t v[64];
-        ptx::tmem_ld_x32(t_row + c * 64, v);
-        ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
-        ptx::tmem_wait_ld();
-        if (c == BN / 64 - 1) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (CG == 2) ptx::mbar_arrive_cluster(tempty_leader0 + 8u * buf);
-                else ptx::mbar_arrive(tempty_local);
-            }
+        if (ready) {
+            ptx::tmem_ld_x32(t_row + c * 64, v);
+            ptx::tmem_ld_x32(t_row + c * 64 + 32, v + 32);
+            ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = 0u;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            __stcg(reinterpret_cast<float4*>(piece + split_quad_offset<Cfg::BM>(c * 64 + 4 * i, r_local)),
-                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
-    }
-    ptx::named_bar_sync(1, 32 * kEpiWarps);
-    // 2. every piece of the tile (S pieces x CG CTAs) is in
-    const uint32_t pieces = static_cast<uint32_t>(S * CG);
-    bool ready = true;
-    if (etid == 0) {
-        ptx::atom_add_acq_rel_gpu(p.counters + t, 1u);
-        ready = wait_count(p.counters + t, pieces, p.status, kSiteSplitPieces, p.timeout_ns);
-    }
-    if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) return false;
-    // 3. this unit's slice of columns, summed over the pieces in ascending order.
-    // The tile's BN / 8 groups of 8 columns are dealt out to the S units, so
-    // every slice starts on a multiple of 8 (16-byte stores of D, 32-byte fp32
-    // loads) and the slices cover all BN columns for any S <= 8.
-    constexpr int kGroups = BN / 8;
-    const int c_begin = 8 * (j * kGroups / S);
-    const int c_end = 8 * ((j + 1) * kGroups / S);
-    const int64_t grow = tm * Cfg::BM + r_local;    // D row
-    if (grow < p.M) {
-        const float* base = p.partials + t * S * static_cast<int64_t>(BN) * Cfg::BM;
-        switch (S) {
-            case 2: split_k_reduce_row<Cfg, T, 2>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 3: split_k_reduce_row<Cfg, T, 3>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 4: split_k_reduce_row<Cfg, T, 4>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 5: split_k_reduce_row<Cfg, T, 5>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 6: split_k_reduce_row<Cfg, T, 6>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            case 7: split_k_reduce_row<Cfg, T, 7>(base, r_local, c_begin, c_end, n0, grow, p); break;
-            default: split_k_reduce_row<Cfg, T, 8>(base, r_local, c_begin, c_end, n0, grow, p); break;
+        for (int g8 = 0; g8 < 8; ++g8) {
+            const int g = c * 8 + g8;
+            const int dest = split_slice_of(g, kGroups, S);
+            const int quad = 2 * (g - split_group_begin(dest, kGroups, S));
+            const uint32_t dest_cta = static_cast<uint32_t>(dest * Cfg::CG) + rank;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t addr = ptx::mapa(recv_base + split_recv_offset(piece, quad + h, row, slice_quads), dest_cta);
+                ptx::st_cluster_v4(addr, v[8 * g8 + 4 * h], v[8 * g8 + 4 * h + 1], v[8 * g8 + 4 * h + 2],
+                                   v[8 * g8 + 4 * h + 3]);
+            }
         }
     }
-    // 4. the last of the 2 * S * CG arrivals re-arms the counter for the next call
-    ptx::named_bar_sync(1, 32 * kEpiWarps);
-    if (etid == 0) {
-        const uint32_t prev = atomicAdd(p.counters + t, 1u);
-        if (prev == 2u * pieces - 1u) p.counters[t] = 0u;
+}
+
+// Sum of the S partials of this CTA's slice for row `row` (D row grow), in
+// ascending piece order, with the fused transform, written to D.
+template <class Cfg, class T>
+__device__ __forceinline__ void split_k_reduce(const uint8_t* recv, const TiledParams& p, int piece, int row,
+                                               int64_t grow, int64_t n0, int S) {
+    constexpr int kGroups = Cfg::BN / 8;
+    const int slice_quads = 2 * ((kGroups + S - 1) / S);
+    const int g0 = split_group_begin(piece, kGroups, S);
+    const int g1 = split_group_begin(piece + 1, kGroups, S);
+    T* D = static_cast<T*>(p.D);
+    if (grow >= p.M) return;
+#pragma unroll 1
+    for (int g = g0; g < g1; ++g) {
+        const int64_t gcol = n0 + 8 * g;
+        if (gcol >= p.N) break;                       // N % 8 == 0: groups are all in or all out
+        const uint4 cv = p.epi.on ? epi_load_c8<T>(p.epi, grow, gcol, p.M, p.N) : make_uint4(0u, 0u, 0u, 0u);
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        const int quad = 2 * (g - g0);
+#pragma unroll 1
+        for (int i = 0; i < S; ++i) {
+            const float4 lo = *reinterpret_cast<const float4*>(recv + split_recv_offset(i, quad, row, slice_quads));
+            const float4 hi = *reinterpret_cast<const float4*>(recv + split_recv_offset(i, quad + 1, row, slice_quads));
+            acc[0] += lo.x; acc[1] += lo.y; acc[2] += lo.z; acc[3] += lo.w;
+            acc[4] += hi.x; acc[5] += hi.y; acc[6] += hi.z; acc[7] += hi.w;
+        }
+        if (p.epi.on) epi_apply8_c<T>(p.epi, acc, cv, gcol);
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = Elem<T>::pack2(acc[2 * e], acc[2 * e + 1]);
+        *reinterpret_cast<uint4*>(D + grow * static_cast<int64_t>(p.N) + gcol) = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    return true;
 }
 
 // T is the element type of D (and C, bias); F8 selects 8-bit operands
@@ -212,11 +159,18 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // rank = this CTA's rank in its MMA pair (the cluster); rank 0 leads:
-    // it issues the MMAs, which commit to barriers in both CTAs
-    const uint32_t rank = (CG > 1) ? ptx::cluster_ctarank() : 0u;
-    constexpr uint32_t leader = 0;
-    const uint16_t pair_mask = static_cast<uint16_t>((1u << CG) - 1u);
+    // A cluster is one MMA group (a CTA pair, or one CTA), or with split K
+    // (p.ksplit = S > 1) S groups on the same tile.  rank = this CTA's rank in
+    // its pair; piece = its group in the cluster (the K piece with split K);
+    // leader = cluster rank of the group's first CTA, which issues the MMAs
+    // (they commit to barriers in both CTAs of a pair).
+    const bool split = p.ksplit > 1;
+    const int csize = CG * (split ? p.ksplit : 1);
+    const uint32_t crank = (csize > 1) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t rank = crank % CG;
+    const int piece = static_cast<int>(crank / CG);
+    const uint32_t leader = static_cast<uint32_t>(piece * CG);
+    const uint16_t pair_mask = static_cast<uint16_t>(((1u << CG) - 1u) << leader);
 
     const uint32_t bar0 = sbase + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -260,8 +214,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
-    const int64_t cluster_idx = blockIdx.x / CG;
-    const int64_t num_clusters = gridDim.x / CG;
+    const int64_t cluster_idx = blockIdx.x / csize;
+    const int64_t num_clusters = gridDim.x / csize;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -275,7 +229,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters, ++round) {
                 int64_t tm, n0;
                 int nw, kb0, kb1;
-                work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
+                work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
                 // Odd rounds walk K downwards: a round starts on the K blocks the
                 // previous round (on the same tile rows) read last, which are the
                 // ones still in L2.  Only the load order changes (the MMA takes
@@ -323,6 +277,10 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
+        if (split) {   // the epilogue's two exchange barriers
+            ptx::cluster_sync();
+            ptx::cluster_sync();
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         // The whole warp runs the loop, so every value it computes is
@@ -336,7 +294,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int64_t u = cluster_idx; ok && u < p.num_units; u += num_clusters, ++it) {
                 int64_t tm, n0;
                 int nw, kb0, kb1;
-                work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
+                work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
                 const uint32_t idesc = ptx::instr_desc(Cfg::BM, nw, p.ab_format);
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
@@ -386,6 +344,30 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();
             wait_phase_warp(drain_bar, 0, p.status, kSiteMmaDrain, p.timeout_ns);
         }
+        if (split) {   // the epilogue's two exchange barriers
+            ptx::cluster_sync();
+            ptx::cluster_sync();
+        }
+    } else if (split) {
+        // ------------------------------------------------------------ epilogue, split K
+        // One tile per cluster (the planner launches exactly one cluster per
+        // tile).  Every thread reaches both barriers, whatever happened before.
+        const int q = warp & 3;
+        const int row = q * 32 + lane;    // this CTA's accumulator row (TMEM lane)
+        const int64_t u = cluster_idx;
+        int64_t tm = 0, n0 = 0;
+        int nw = 0, kb0 = 0, kb1 = 0;
+        if (u < p.num_units) work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
+        const bool ready = u < p.num_units &&
+                           wait_phase_warp(tfull_bar(0), 0, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
+        if (ready) ptx::tc_fence_after();
+        // A: every MMA of the cluster is done, so every operand ring is free
+        ptx::cluster_sync();
+        split_k_send<Cfg>(sbase, tmem_base + (static_cast<uint32_t>(q * 32) << 16), ready, piece, rank, row,
+                          p.ksplit);
+        // B: every partial of this CTA's slice is in its receive buffer
+        ptx::cluster_sync();
+        if (ready) split_k_reduce<Cfg, T>(smem, p, piece, row, tm * Cfg::BM + rank * 128 + row, n0, p.ksplit);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;    // TMEM lanes 32q .. 32q+31 are readable by this warp
@@ -401,7 +383,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int64_t u = cluster_idx; u < p.num_units; u += num_clusters, ++it) {
             int64_t tm, n0;
             int nw, kb0, kb1;
-            work_unit(u, p, Cfg::BN, tm, n0, nw, kb0, kb1);
+            work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
             const int chunks = nw / Cfg::EPI_COLS;
             const uint32_t buf = it & 1u;
             const uint32_t use = (it >> 1) & 1u;
@@ -409,28 +391,16 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // accumulator is waited for (ev[0] always holds the current chunk's)
             constexpr int kChunks = Cfg::BN / Cfg::EPI_COLS;
             EpiCols64<T> ev[kChunks];
-            if (p.epi.on && p.ksplit == 1) {
+            if (p.epi.on) {
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
                     if (c < chunks) ev[c].load(p.epi, n0 + c * Cfg::EPI_COLS, lane, p.N);
             }
-            if (p.ksplit > 1) {
-                // all four epilogue warps decide together: they meet at named barriers
-                const bool ready = wait_phase(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
-                if (!ptx::named_bar_and(1, 32 * kEpiWarps, ready)) break;
-            } else if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) {
-                break;
-            }
+            if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) break;
             ptx::tc_fence_after();
             const int64_t row0 = tm * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
             const bool rows_in = row0 < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
-            if (p.ksplit > 1) {
-                if (!split_k_epilogue<Cfg, T>(p, u, tm, n0, t_row, tempty_leader0, tempty_bar(buf), buf, q, lane,
-                                           threadIdx.x - 64, rank))
-                    break;
-                continue;
-            }
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 const int64_t col0 = n0 + c * Cfg::EPI_COLS;

@@ -18,6 +18,8 @@ struct TiledOps {
     cudaError_t (*prepare)();
     // co-resident clusters (cta_group 2) or CTAs per SM (cta_group 1) on the current device
     cudaError_t (*max_active)(int* out);
+    // co-resident split-K clusters of `pieces` MMA groups on the current device
+    cudaError_t (*max_active_split)(int pieces, int* out);
     // b_piece: B with a box of (B rows per CTA) / split rows, for the column
     // pieces of the last round's tiles
     cudaError_t (*launch)(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_piece,

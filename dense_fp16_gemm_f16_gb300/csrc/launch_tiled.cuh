@@ -33,6 +33,21 @@ struct TiledLauncher {
         }
     }
 
+    static cudaError_t max_active_split(int pieces, int* out) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(Cfg::CG * pieces), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(Cfg::CG * pieces);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg, T, F8>, &cfg);
+    }
+
     static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_piece,
                               const CUtensorMap& d, const TiledParams& p, int grid_ctas, cudaStream_t stream) {
         cudaLaunchConfig_t cfg = {};
@@ -47,9 +62,11 @@ struct TiledLauncher {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 1;
-        if constexpr (Cfg::CG > 1) {
+        // clusters: a CTA pair, or with split K ksplit MMA groups on one tile
+        const int cluster = Cfg::CG * (p.ksplit > 1 ? p.ksplit : 1);
+        if (cluster > 1) {
             attr[1].id = cudaLaunchAttributeClusterDimension;
-            attr[1].val.clusterDim.x = Cfg::CG;
+            attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
             attr[1].val.clusterDim.y = 1;
             attr[1].val.clusterDim.z = 1;
             cfg.numAttrs = 2;
@@ -61,7 +78,7 @@ struct TiledLauncher {
     static const TiledOps& ops() {
         static const TiledOps o = {Cfg::CG, Cfg::BM, Cfg::BN, Cfg::STAGES, Cfg::SMEM_BYTES,
                                    Cfg::TMEM_COLS, Cfg::CG, Cfg::B_ROWS,
-                                   &prepare, &max_active, &launch};
+                                   &prepare, &max_active, &max_active_split, &launch};
         return o;
     }
 };

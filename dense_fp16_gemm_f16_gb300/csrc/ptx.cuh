@@ -92,6 +92,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr_cluster, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr_cluster), "f"(v) : "memory");
 }
 
+// 16-byte store (four 32-bit words) to shared memory given by its
+// shared::cluster address (this or a peer CTA of the cluster).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr_cluster, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr_cluster), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");

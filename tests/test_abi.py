@@ -172,10 +172,10 @@ def test_plans_for_the_named_workloads(lib):
     # 16 pair tiles but a short K loop (32 blocks): 128x256 tiles in quarters
     assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1
     p = P(512, 2048, 8192)
-    # 16 pair tiles fill less than half of the 76 pairs and K is long: each
-    # tile's K loop is split over 4 pairs (32 K blocks each), 64 units on 128 SMs
+    # 16 pair tiles and a long K loop: each tile's K loop split over a cluster of
+    # 4 pairs (32 K blocks each), 16 clusters of 8 CTAs, no workspace
     assert p["variant"] == "TILE_2CTA_SPLITK" and (p["k_split"], p["grid_ctas"]) == (4, 128)
-    assert p["workspace_bytes"] >= 16 * 4 * 256 * 256 * 4 + 16 * 4
+    assert p["workspace_bytes"] == 0
     p = P(1024, 1024, 2048, variant=g.Variant.TILE_2CTA_SPLITK)        # asked for explicitly: split
     assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
     p = P(2048, 2048, 2048)
@@ -257,17 +257,21 @@ def test_tail_split_minimises_the_last_round(lib):
 
 def test_ksplit_choice(lib):
     P = lambda *a, **k: g.gemm_f16_nt_plan(*a, num_sms=152, **k)  # noqa: E731
-    # pieces per tile: at most 8, every unit resident at once, >= 4 K blocks each
+    # pieces per tile: at most 4 (clusters of at most 8 CTAs), one wave of
+    # clusters (152 SMs: 38 clusters of 2 pairs, 25 of 3, 19 of 4), >= 4 K blocks each
     V = g.Variant.TILE_2CTA_SPLITK
-    assert P(256, 256, 64 * 64, variant=V)["k_split"] == 8
+    assert P(256, 256, 64 * 64, variant=V)["k_split"] == 4
     assert P(256, 256, 64 * 12, variant=V)["k_split"] == 3
     assert P(256, 256, 64 * 7, variant=V)["k_split"] == 1                # under 4 K blocks per piece: no split
-    q = P(256 * 4, 256 * 5, 64 * 64, variant=V)                           # 20 tiles: 3 pieces fit on 76 pairs
+    q = P(256 * 4, 256 * 5, 64 * 64, variant=V)                           # 20 tiles: 25 clusters of 3 pairs fit
     assert q["k_split"] == 3 and q["grid_ctas"] == 2 * 20 * 3
-    # AUTO splits only where the K blocks a split saves, kb * (1 - 1/S), reach 56
-    assert P(256, 256, 64 * 63)["k_split"] == 1 and P(256, 256, 64 * 64)["k_split"] == 8
-    assert P(1024, 2048, 64 * 80)["variant"] == "TILE_2CTA_256x256"     # S = 2 saves 40 blocks: unsplit
-    assert P(768, 2048, 64 * 96)["k_split"] == 3                          # S = 3 saves 64 blocks: split
+    q = P(256 * 8, 256 * 5, 64 * 64, variant=V)                           # 40 tiles: too many for one wave
+    assert q["variant"] == "TILE_2CTA_256x256" and q["k_split"] == 1
+    # AUTO splits only where the K blocks a split saves, kb * (1 - 1/S), reach 40
+    assert P(256, 256, 64 * 53)["k_split"] == 1 and P(256, 256, 64 * 54)["k_split"] == 4
+    assert P(1024, 2048, 64 * 78)["variant"] == "TILE_2CTA_256x256"     # S = 2 saves 39 blocks: unsplit
+    assert P(1024, 2048, 64 * 80)["k_split"] == 2                         # S = 2 saves 40 blocks: split
+    assert P(768, 2048, 64 * 96)["k_split"] == 3                          # 24 tiles: 25 clusters of 3 pairs fit
 
 
 def test_plans_for_8bit_operands(lib):
@@ -287,9 +291,9 @@ def test_plans_for_8bit_operands(lib):
     p = P(16, 8192, 8192)
     assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and (p["k_split"], p["n_tiles"]) == (2, 76)
     p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: a split by 4
-    assert p["variant"] == "TILE_2CTA_256x256" and p["k_split"] == 1     # would save only 48: unsplit pairs
-    p = P(512, 1024, 16384)                                  # 128 K blocks over 8 pieces: split
-    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 8
+    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4      # saves 48 blocks: split
+    p = P(512, 1024, 16384)                                  # 128 K blocks over 4 pieces: split
+    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
     assert g.gemm_nt_plan_ex(g.Dtype.F16, 8192, 8192, 8192, num_sms=152) == \
         g.gemm_f16_nt_plan(8192, 8192, 8192, num_sms=152)
     assert g.gemm_nt_plan_ex(g.Dtype.E5M2, 8192, 8192, 8192, num_sms=152)["tile_k"] == 128

@@ -40,26 +40,56 @@ def _bf16_host(t):
 
 
 def test_concurrent_streams_own_workspaces():
-    # split-K pair tiles on one stream and the small-M split kernel on another,
-    # enqueued alternately: both keep fp32 partials and counters in their own
-    # stream's workspace while their kernels overlap
+    # split-K pair tiles on one stream and the small-M kernels on others,
+    # enqueued alternately while their kernels overlap: the stream-K small-M
+    # kernel keeps fp32 partials and counters in its own stream's workspace
     A1, B1 = inputs.operands(512, 2048, 2048, seed=51)
     A2, B2 = inputs.operands(16, 4096, 4096, "normal:1", "normal:1/sqrtK", seed=52)
     dA1, dB1, dA2, dB2 = _f16(A1), _f16(B1), _f16(A2), _f16(B2)
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     D1 = [torch.full((512, 2048), float("nan"), dtype=torch.float16, device="cuda") for _ in range(2)]
     D2 = [torch.full((16, 4096), float("nan"), dtype=torch.float16, device="cuda") for _ in range(2)]
+    D3 = [torch.full((16, 4096), float("nan"), dtype=torch.float16, device="cuda") for _ in range(2)]
     torch.cuda.synchronize()
     for i in range(12):
         g.gemm_f16_nt_variant(dA1, dB1, D1[i % 2], variant=g.Variant.TILE_2CTA_SPLITK, stream=s1)
         g.gemm_f16_nt_variant(dA2, dB2, D2[i % 2], variant=g.Variant.SKINNY_SPLITK, stream=s2)
+        g.gemm_f16_nt_variant(dA2, dB2, D3[i % 2], variant=g.Variant.SKINNY_STREAMK, stream=s3)
     g.gemm_f16_nt_check(stream=s1)
     g.gemm_f16_nt_check(stream=s2)
+    g.gemm_f16_nt_check(stream=s3)
     ref1, ref2 = oracle.gemm(A1, B1), oracle.gemm(A2, B2)
     for d in D1:
         check_close(d.cpu().numpy(), ref1, 2048, "split-K on stream 1")
     for d in D2:
         check_close(d.cpu().numpy(), ref2, 4096, "small-M on stream 2")
+    for d in D3:
+        check_close(d.cpu().numpy(), ref2, 4096, "stream-K small-M on stream 3")
+
+
+def test_two_split_k_calls_on_unordered_streams():
+    # Two split-K calls, each with as many tiles as one wave of its clusters
+    # holds (all pair slots), on two streams with no ordering between them, so
+    # the second grid's clusters must wait for SMs the first one holds.  Every
+    # cluster sums its own tile's pieces and waits on no other cluster, so both
+    # finish, match the oracle, and no wait runs out.
+    M, N, K = 1024, 1024, 4096                 # 16 pair tiles, K split over each tile's cluster
+    plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.TILE_2CTA_SPLITK)
+    assert plan["variant"] == "TILE_2CTA_SPLITK" and plan["k_split"] > 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 2 * plan["grid_ctas"] > sms          # together the two grids do not fit at once
+    ops = [inputs.operands(M, N, K, seed=60 + i) for i in range(2)]
+    dev = [(_f16(a), _f16(b)) for a, b in ops]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    Ds = [torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i in range(2):
+            g.gemm_f16_nt_variant(dev[i][0], dev[i][1], Ds[i], variant=g.Variant.TILE_2CTA_SPLITK, stream=streams[i])
+    for i in range(2):
+        g.gemm_f16_nt_check(stream=streams[i])   # raises on a timeout
+    for i, (a, b) in enumerate(ops):
+        check_close(Ds[i].cpu().numpy(), oracle.gemm(a, b), K, f"split-K on unordered stream {i}")
 
 
 def test_cuda_graph_capture_and_replay():
