@@ -682,6 +682,13 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         const size_t partial_bytes = static_cast<size_t>(pl.grid_ctas) * pl.max_tiles_per_cta * ops.mn * 128 * 4;
         st = get_workspace(dev_id, stream, partial_bytes, static_cast<size_t>(pl.n_tiles), &ws);
         if (st != GEMM_OK) return st;
+        // Every completed call leaves the tile counters at zero, but one that
+        // gave up waiting (a timeout) may not; clear them on the stream so a
+        // later call never starts from counts an earlier one left behind.
+        if (cudaMemsetAsync(ws->counters, 0, static_cast<size_t>(pl.n_tiles) * sizeof(uint32_t), s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
         StreamKParams p;
         p.M = static_cast<int32_t>(M);
         p.N = static_cast<int32_t>(N);
