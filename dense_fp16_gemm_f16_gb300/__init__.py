@@ -42,6 +42,7 @@ class Variant(enum.IntEnum):
     SKINNY_SPLITK = 4
     TILE_2CTA_SPLITK = 5
     SKINNY_STREAMK = 6
+    TILE_2CTA_512x256 = 7
 
 
 class Dtype(enum.IntEnum):

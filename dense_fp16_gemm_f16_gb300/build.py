@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgemm_f16.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "tiled_2cta.cu", "tiled_1cta.cu", "skinny.cu", "streamk.cu"]
+SOURCES = ["api.cu", "tiled_2cta.cu", "tiled_2cta512.cu", "tiled_1cta.cu", "skinny.cu", "streamk.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                            "-I", INCLUDE, "-I", CSRC]

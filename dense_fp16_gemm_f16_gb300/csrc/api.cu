@@ -53,6 +53,7 @@ struct DeviceState {
     int sms = 0;
     uint32_t* status = nullptr;
     int max_clusters_2cta = 0;   // co-resident 2-CTA clusters of the 256x256 kernel
+    int max_clusters_2cta2c = 0; // co-resident 2-CTA clusters of the two-consumer 512x256 kernel
     int per_sm_1cta128 = 0;      // co-resident CTAs per SM
     int per_sm_1cta256 = 0;
     int skinny_clusters[kSkinnyMaxPieces + 1] = {};   // co-resident small-M clusters of P CTAs
@@ -107,6 +108,18 @@ constexpr int64_t kPairMinBlocks = 48;
 // 43.4), and from 16 blocks on the pairs win in both.
 constexpr int64_t kShortKBlocks16 = 8;
 constexpr int64_t kShortKBlocks8 = 12;
+// When a row of K elements is not a whole number of 32-byte sectors, every
+// other row of A and B starts 16 bytes into a sector, each 128-byte TMA row
+// touches five sectors, and L2 delivery (not DRAM, not the tensor pipe)
+// bounds the pair kernel (ncu at 4000 x 11000 x 4104: DRAM traffic 1.01x the
+// compulsory bytes, tensor pipe idle a third of its active cycles).  The
+// two-consumer kernel stages B once for 512 rows instead of 256, a quarter
+// less operand traffic per FLOP, and wins there despite its single-buffered
+// accumulators, given at least two rounds of its 512 x 256 tiles (GB300,
+// back-to-back launches, pairs against two consumers: 4000 x 11000 x 4104
+// 250-265 / 243-256 us, K = 4136 270-274 / 257-258, 6144 x 6144 x 6152 354 /
+// 311; with rows on sectors the pairs win: 8192^3 533-555 / 567-578,
+// 4000 x 11000 x 4112 221-230 / 253-255).
 
 int64_t raster_group(int64_t m_tiles, int tile_m, int64_t K, int in_bytes) {
 #ifdef GEMM_GROUP_M
@@ -144,6 +157,7 @@ uint32_t dtype_ab_format(int dtype) {
 struct Limits {
     int sms;
     int max_clusters_2cta;
+    int max_clusters_2cta2c;
     int per_sm_1cta128;
     int per_sm_1cta256;
     int skinny_clusters[kSkinnyMaxPieces + 1];   // index P: co-resident clusters of P CTAs (0: unknown)
@@ -152,7 +166,7 @@ struct Limits {
 
 // A pure-host planner's view of a GPU with `sms` SMs (nothing queried).
 Limits host_limits(int sms) {
-    Limits lim{sms, sms / 2, 1, 1, {}, {}};
+    Limits lim{sms, sms / 2, sms / 2, 1, 1, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; pc *= 2) lim.skinny_clusters[pc] = sms / pc;
     for (int s = 1; s <= kSplitMaxPieces; ++s) lim.split_clusters[s] = sms / (2 * s);
     return lim;
@@ -227,6 +241,7 @@ const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
     switch (v) {
         case GEMM_VARIANT_TILE_1CTA_128x128: return tiled_ops_1cta128(dtype);
         case GEMM_VARIANT_TILE_1CTA_128x256: return tiled_ops_1cta256(dtype);
+        case GEMM_VARIANT_TILE_2CTA_512x256: return tiled_ops_2cta512(dtype);
         default: return tiled_ops_2cta256(dtype);   // TILE_2CTA_256x256, TILE_2CTA_SPLITK
     }
 }
@@ -237,7 +252,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     const gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
     const int64_t bk = stage_k(in_bytes);
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_STREAMK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_512x256) return GEMM_ERR_INVALID_VALUE;
     if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
         return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
@@ -262,6 +277,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             const int ks = choose_ksplit(t2, lim.split_clusters, kb);
             if (t2 >= pairs && kb <= (in_bytes == 1 ? kShortKBlocks8 : kShortKBlocks16))
                 variant = GEMM_VARIANT_TILE_1CTA_128x256;
+            else if (t2 >= pairs && (K * in_bytes) % 32 != 0 && cdiv(M, 512) * cdiv(N, 256) >= 2 * pairs)
+                variant = GEMM_VARIANT_TILE_2CTA_512x256;
             else if (t2 >= pairs)
                 variant = GEMM_VARIANT_TILE_2CTA_256x256;
             else if (ks > 1 && kb * (ks - 1) >= kSplitKSavedBlocks * ks)
@@ -344,7 +361,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     // slots = clusters (or CTAs) that can be resident at once
     int64_t slots;
     if (ops.cta_group == 2) {
-        slots = lim.max_clusters_2cta > 0 ? lim.max_clusters_2cta : lim.sms / 2;
+        const int c = variant == GEMM_VARIANT_TILE_2CTA_512x256 ? lim.max_clusters_2cta2c : lim.max_clusters_2cta;
+        slots = c > 0 ? c : lim.sms / 2;
     } else {
         const int per_sm = variant == GEMM_VARIANT_TILE_1CTA_128x128 ? lim.per_sm_1cta128 : lim.per_sm_1cta256;
         slots = static_cast<int64_t>(lim.sms) * (per_sm > 0 ? per_sm : 1);
@@ -414,7 +432,8 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
         }
         const TiledOps* tiled[3] = {&tiled_ops_2cta256(0), &tiled_ops_1cta128(0), &tiled_ops_1cta256(0)};
         for (int dt : {0, 1, 2}) {   // fp16, bf16, 8-bit (one kernel for both formats)
-            const TiledOps* all[3] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt)};
+            const TiledOps* all[4] = {&tiled_ops_2cta256(dt), &tiled_ops_1cta128(dt), &tiled_ops_1cta256(dt),
+                                      &tiled_ops_2cta512(dt)};
             for (const TiledOps* t : all)
                 if (t->prepare() != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
             for (int mn : {16, 32, 64})
@@ -423,15 +442,16 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
                     return GEMM_ERR_CUDA;
                 }
         }
-        int clusters = 0, per128 = 0, per256 = 0;
+        int clusters = 0, per128 = 0, per256 = 0, clusters2c = 0;
         if (tiled[0]->max_active(&clusters) != cudaSuccess || tiled[1]->max_active(&per128) != cudaSuccess ||
-            tiled[2]->max_active(&per256) != cudaSuccess) {
+            tiled[2]->max_active(&per256) != cudaSuccess || tiled_ops_2cta512(0).max_active(&clusters2c) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         d.sms = sms;
         d.status = static_cast<uint32_t*>(status);
         d.max_clusters_2cta = clusters;
+        d.max_clusters_2cta2c = clusters2c;
         d.per_sm_1cta128 = per128;
         d.per_sm_1cta256 = per256;
         // co-resident clusters of each size the planner may use (a size the
@@ -458,7 +478,7 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    Limits lim{d.sms, d.max_clusters_2cta, d.per_sm_1cta128, d.per_sm_1cta256, {}, {}};
+    Limits lim{d.sms, d.max_clusters_2cta, d.max_clusters_2cta2c, d.per_sm_1cta128, d.per_sm_1cta256, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; ++pc) lim.skinny_clusters[pc] = d.skinny_clusters[pc];
     for (int sp = 1; sp <= kSplitMaxPieces; ++sp) lim.split_clusters[sp] = d.split_clusters[sp];
     return lim;
@@ -603,7 +623,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
             if (epi.scale_n && ranges_overlap(epi.scale_n, N * 4, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_SKINNY_STREAMK) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_512x256) return GEMM_ERR_INVALID_VALUE;
     if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
         return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;

@@ -48,22 +48,37 @@ GEMM_HD int64_t div_nonneg(int64_t a, int64_t b) {
 
 // ------------------------------------------------------------------ tiled
 // Persistent, warp-specialised kernel.  CG = CTAs per MMA (1, or 2 for a
-// cta_group::2 pair in a 2-CTA cluster), BN = output columns per tile.  A tile
-// is BM = 128*CG rows by BN columns; each CTA of a pair loads its own 128 rows
-// of A and its own BN/CG rows of B and owns 128 accumulator rows in its TMEM.
-// Reuse of A and B blocks between tiles comes from L2 (grouped raster below).
-template <int CG_, int BN_, int STAGES_>
+// cta_group::2 pair in a 2-CTA cluster), BN = output columns per tile.  With
+// one consumer a tile is 128*CG rows by BN columns; each CTA of a pair loads
+// its own 128 rows of A and its own BN/CG rows of B and owns 128 accumulator
+// rows in its TMEM.  Reuse of A and B blocks between tiles comes from L2
+// (grouped raster below).
+// CONS = MMA consumers per CTA sharing each staged B tile ("Building a Tiled
+// GEMM", optimisation roadmap, last item): with 2, each CTA stages 2 x 128 rows
+// of A and its BN/CG rows of B once, and two MMAs per K step (one per 128-row
+// half of A) feed two accumulators -- a tile of 2*128*CG rows -- each drained
+// by its own epilogue warpgroup.  B then crosses from L2 once for twice the
+// rows, a quarter less operand traffic per FLOP; the two accumulators fill
+// TMEM, so they are single-buffered and the epilogue no longer hides under
+// the next tile's MMAs.
+template <int CG_, int BN_, int STAGES_, int CONS_ = 1>
 struct TiledConfig {
     static constexpr int CG = CG_;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
-    static constexpr int BM = 128 * CG;
-    static constexpr int A_ROWS = 128;
+    static constexpr int CONS = CONS_;
+    static constexpr int MMA_M = 128 * CG;                   // rows of one MMA
+    static constexpr int BM = MMA_M * CONS;                  // rows of a tile
+    static constexpr int A_ROWS = 128 * CONS;                // per CTA
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = A_ROWS * kStageRowBytes;
+    static constexpr int A_HALF_BYTES = 128 * kStageRowBytes;   // one consumer's A rows
     static constexpr int B_BYTES = B_ROWS * kStageRowBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
-    static constexpr int TMEM_COLS = 2 * BN;                 // two accumulator buffers
+    static constexpr int EPI_WARPS = kEpiWarps * CONS;      // one warpgroup per consumer
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int ACC_BUFS = CONS == 1 ? 2 : 1;       // accumulator buffers per consumer
+    static constexpr int TMEM_COLS = ACC_BUFS * CONS * BN;
     static constexpr int EPI_COLS = 64;                      // columns per TMA store box
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // one warp's 32 rows
     // The operand ring holds STAGES whole stages of [A tile | B tile].  A launch
@@ -74,7 +89,7 @@ struct TiledConfig {
     static constexpr int MAX_SPLIT = (BN / 64 < 4) ? BN / 64 : 4;
     static constexpr int MAX_STAGES = RING_BYTES / (A_BYTES + B_BYTES / MAX_SPLIT);
     static constexpr int OFF_EPI = RING_BYTES;
-    static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 2 * EPI_BUF_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
     // full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2], drain
     static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
@@ -82,8 +97,9 @@ struct TiledConfig {
     // of the chunk it is writing, read back by every lane as broadcasts
     static constexpr int COLS_BYTES = EPI_COLS * 4 + EPI_COLS * 2;
     static constexpr int OFF_COLS = (OFF_SLOT + 16 + 15) / 16 * 16;
-    static constexpr int SMEM_BYTES = OFF_COLS + kEpiWarps * COLS_BYTES + 1024;  // + slack to align the base
+    static constexpr int SMEM_BYTES = OFF_COLS + EPI_WARPS * COLS_BYTES + 1024;  // + slack to align the base
     static_assert(A_BYTES % 1024 == 0 && (B_BYTES / MAX_SPLIT) % 1024 == 0, "stage tiles must stay 1024-aligned");
+    static_assert(CONS == 1 || CONS == 2, "one or two consumers");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 up to 256");
     static_assert(B_ROWS <= 256, "TMA box rows are limited to 256");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
@@ -91,6 +107,7 @@ struct TiledConfig {
 };
 
 using Cfg2cta256 = TiledConfig<2, 256, 6>;
+using Cfg2cta512 = TiledConfig<2, 256, 3, 2>;   // two consumers: 512 x 256 per pair
 using Cfg1cta128 = TiledConfig<1, 128, 6>;
 using Cfg1cta256 = TiledConfig<1, 256, 4>;
 

@@ -143,11 +143,12 @@ __device__ __forceinline__ void split_k_reduce(const uint8_t* recv, const TiledP
 // T is the element type of D (and C, bias); F8 selects 8-bit operands
 // (kind::f8f6f4, 128 K elements per stage) instead of 16-bit ones of type T.
 template <class Cfg, class T, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBpiece, const __grid_constant__ CUtensorMap tmD,
                   const TiledParams p) {
     constexpr int CG = Cfg::CG;
+    constexpr int CONS = Cfg::CONS;
     constexpr int MAXS = Cfg::MAX_STAGES;
     constexpr int kStageK = stage_k(F8 ? 1 : 2);
     extern __shared__ uint8_t smem_raw[];
@@ -194,7 +195,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);                 // one MMA commit
-            ptx::mbar_init(tempty_bar(b), kEpiWarps * CG);   // every epilogue warp of the pair
+            ptx::mbar_init(tempty_bar(b), Cfg::EPI_WARPS * CG);   // every epilogue warp of the pair
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::fence_mbar_init();
@@ -238,7 +239,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // each CTA of a pair supplies nw / CG rows of B to the MMA; a
                 // column piece of a tail tile loads only those rows (box of the
                 // second B map) instead of the whole tile's
-                const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * Cfg::A_ROWS);
+                // A rows of consumer h: tile row tm * BM + h * MMA_M + rank * 128
+                const int32_t a_row = static_cast<int32_t>(tm * Cfg::BM + rank * 128);
                 const int32_t b_row = static_cast<int32_t>(n0 + rank * (nw / CG));
                 const bool piece = nw < Cfg::BN;
                 const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
@@ -255,14 +257,20 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (ptx::elect_one()) {
                         if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-                            ptx::tma_load_2d(a_dst, &tmA, full_bar(stage), kx, a_row);
+#pragma unroll
+                            for (int h = 0; h < CONS; ++h)
+                                ptx::tma_load_2d(a_dst + h * Cfg::A_HALF_BYTES, &tmA, full_bar(stage), kx,
+                                                 a_row + h * Cfg::MMA_M);
                             ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kx, b_row);
                         } else {
                             // Both CTAs' bytes complete on the leader's full barrier; the
                             // leader announces the pair's total.
                             const uint32_t leader_full = ptx::mapa(full_bar(stage), leader);
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
-                            ptx::tma_load_2d_pair(a_dst, &tmA, leader_full, kx, a_row);
+#pragma unroll
+                            for (int h = 0; h < CONS; ++h)
+                                ptx::tma_load_2d_pair(a_dst + h * Cfg::A_HALF_BYTES, &tmA, leader_full, kx,
+                                                      a_row + h * Cfg::MMA_M);
                             ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kx, b_row);
                         }
                     }
@@ -295,15 +303,16 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 int64_t tm, n0;
                 int nw, kb0, kb1;
                 work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
-                const uint32_t idesc = ptx::instr_desc(Cfg::BM, nw, p.ab_format);
-                const uint32_t buf = it & 1u;
-                const uint32_t use = (it >> 1) & 1u;
+                const uint32_t idesc = ptx::instr_desc(Cfg::MMA_M, nw, p.ab_format);
+                // accumulator buffer (two per consumer, alternating) and its use count
+                const uint32_t buf = Cfg::ACC_BUFS == 2 ? (it & 1u) : 0u;
+                const uint32_t use = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
                 if (!wait_phase_warp(tempty_bar(buf), use ^ 1u, p.status, kSiteMmaTmemEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * Cfg::BN;
+                const uint32_t d_tmem = tmem_base + buf * CONS * Cfg::BN;   // consumer h adds h * BN
                 // the producer's K order for this unit (odd rounds walk K downwards)
                 const bool reverse = (it & 1u) && p.ksplit == 1;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -319,11 +328,14 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int blk = reverse ? (kb1 - 1 - (kb - kb0)) : kb;
                     const int steps = (blk == p.k_blocks - 1) ? p.last_k_steps : kMmaPerStage;
                     if (ptx::elect_one()) {
+                        // each consumer's MMAs read its own 128 rows of A and the shared B
 #pragma unroll
-                        for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
-                            if (k < steps)
-                                ptx::mma<CG, F8>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                                 (kb != kb0 || k != 0) ? 1u : 0u);
+                        for (int h = 0; h < CONS; ++h)
+#pragma unroll
+                            for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
+                                if (k < steps)
+                                    ptx::mma<CG, F8>(d_tmem + h * Cfg::BN, a_desc + h * (Cfg::A_HALF_BYTES >> 4) + 2u * k,
+                                                     b_desc + 2u * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
                         if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
                         else ptx::mma_commit_pair(empty_bar(stage), pair_mask);
                     }
@@ -372,6 +384,7 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;    // TMEM lanes 32q .. 32q+31 are readable by this warp
         const int ew = warp - 2;   // owner of staging buffers 2ew, 2ew+1
+        const int h = ew / kEpiWarps;   // the consumer (accumulator) this warp drains
         const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(tempty_bar(0), leader) : tempty_bar(0);
         // which parts of the fused transform run (warp-uniform, for the whole launch)
         const bool epi_c = p.epi.on && p.epi.C != nullptr && p.epi.beta != 0.0f;
@@ -385,8 +398,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int nw, kb0, kb1;
             work_unit(u, p, Cfg::BN, piece, tm, n0, nw, kb0, kb1);
             const int chunks = nw / Cfg::EPI_COLS;
-            const uint32_t buf = it & 1u;
-            const uint32_t use = (it >> 1) & 1u;
+            const uint32_t buf = Cfg::ACC_BUFS == 2 ? (it & 1u) : 0u;
+            const uint32_t use = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
             // the per-column scales and bias of the whole unit, fetched before its
             // accumulator is waited for (ev[0] always holds the current chunk's)
             constexpr int kChunks = Cfg::BN / Cfg::EPI_COLS;
@@ -398,9 +411,9 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) break;
             ptx::tc_fence_after();
-            const int64_t row0 = tm * Cfg::BM + rank * 128 + q * 32;  // D row of lane 0
+            const int64_t row0 = tm * Cfg::BM + h * Cfg::MMA_M + rank * 128 + q * 32;  // D row of lane 0
             const bool rows_in = row0 < p.M;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::BN;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (buf * CONS + h) * Cfg::BN;
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 const int64_t col0 = n0 + c * Cfg::EPI_COLS;

@@ -46,6 +46,7 @@ struct StreamKOps {
 // dtype: 0 = fp16 operands and output, 1 = bf16, 2 / 3 = E4M3 / E5M2 operands
 // with a bf16 output
 const TiledOps& tiled_ops_2cta256(int dtype);
+const TiledOps& tiled_ops_2cta512(int dtype);   // two consumers per CTA
 const TiledOps& tiled_ops_1cta128(int dtype);
 const TiledOps& tiled_ops_1cta256(int dtype);
 const SkinnyOps& skinny_ops(int mn, int dtype);    // mn = 16, 32 or 64

@@ -17,7 +17,7 @@ struct TiledLauncher {
         if constexpr (Cfg::CG > 1) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(Cfg::CG, 1, 1);
-            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
             cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -28,7 +28,7 @@ struct TiledLauncher {
             cfg.numAttrs = 1;
             return cudaOccupancyMaxActiveClusters(out, gemm_tiled_kernel<Cfg, T, F8>, &cfg);
         } else {
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg, T, F8>, kThreads,
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_tiled_kernel<Cfg, T, F8>, Cfg::THREADS,
                                                                  Cfg::SMEM_BYTES);
         }
     }
@@ -36,7 +36,7 @@ struct TiledLauncher {
     static cudaError_t max_active_split(int pieces, int* out) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(Cfg::CG * pieces), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -52,7 +52,7 @@ struct TiledLauncher {
                               const CUtensorMap& d, const TiledParams& p, int grid_ctas, cudaStream_t stream) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
         // programmatic stream serialisation: this grid may be scheduled while the

@@ -91,10 +91,13 @@ typedef enum {
                                            several CTA pairs (for shapes with few tiles); falls
                                            back to GEMM_VARIANT_TILE_2CTA_256x256 when the tiles
                                            already fill the GPU */,
-    GEMM_VARIANT_SKINNY_STREAMK = 6     /* M <= 64: operands swapped; (tile, K block) units dealt
+    GEMM_VARIANT_SKINNY_STREAMK = 6,    /* M <= 64: operands swapped; (tile, K block) units dealt
                                            in equal contiguous ranges to all SMs, split tiles
                                            summed through the fp32 workspace (the kernel of
                                            gemm_f16_nt_noalloc) */
+    GEMM_VARIANT_TILE_2CTA_512x256 = 7  /* persistent, 2-CTA cluster, 512x256 tile per pair: two
+                                           MMA consumers per CTA share each staged B tile, each
+                                           with its own accumulator and epilogue warpgroup */
 } gemm_variant_t;
 
 /* Element type of A and B; both operands share it and the MMA accumulates in

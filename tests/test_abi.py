@@ -64,7 +64,7 @@ def test_argument_errors_are_returned_before_any_device_call(lib):
     assert _call(8, -8, 8) == S.ERR_INVALID_VALUE
     assert _call(8, 8, -8) == S.ERR_INVALID_VALUE
     assert _call(2 ** 31, 8, 8) == S.ERR_INVALID_VALUE
-    assert _call(8, 8, 8, variant=7) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, 8, variant=8) == S.ERR_INVALID_VALUE
     assert _call(65, 8, 8, variant=g.Variant.SKINNY_SPLITK) == S.ERR_INVALID_VALUE
     assert _call(65, 8, 8, variant=g.Variant.SKINNY_STREAMK) == S.ERR_INVALID_VALUE
     # empty problems are a no-op even with NULL pointers
@@ -162,12 +162,19 @@ def test_plans_for_the_named_workloads(lib):
     # at most 12 tile rows (12 x 256 rows x 16 KB = 48 MiB of A) per group: 32 rows in 3 groups of 11
     assert p["group_m"] == 11
     p = P(4000, 11000, 4104)
-    # the pair kernel on all 152 SMs, ragged in M, N and K (the last K block 8 wide)
-    assert p["variant"] == "TILE_2CTA_256x256" and p["grid_ctas"] == 152
-    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 43, 65)
-    assert (p["num_full_tiles"], p["tail_split"]) == (684, 4)           # 9 rounds of 76 + 4 tiles in quarters
-    assert p["group_m"] == 16                                           # all of A (32 MiB) in one group
-    assert P(4000, 11000, 4112)["variant"] == "TILE_2CTA_256x256"
+    # K = 4104: rows are not whole 32-byte sectors, so two MMA consumers per CTA
+    # share each staged B tile, 512 x 256 per pair, on all 152 SMs; ragged in
+    # M, N and K (the last K block 8 wide)
+    assert p["variant"] == "TILE_2CTA_512x256" and p["grid_ctas"] == 152 and p["tile_m"] == 512
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (8, 43, 65)
+    assert (p["num_full_tiles"], p["tail_split"]) == (304, 1)           # 4 rounds of 76 + 40 tiles whole
+    assert p["group_m"] == 8                                            # all of A (32 MiB) in one group
+    # rows on 32-byte sectors: the pair kernel with double-buffered accumulators
+    q = P(4000, 11000, 4112)
+    assert q["variant"] == "TILE_2CTA_256x256"
+    assert (q["m_tiles"], q["num_full_tiles"], q["tail_split"], q["group_m"]) == (16, 684, 4, 16)
+    # misaligned, but under two rounds of 512 x 256 tiles: the pair kernel
+    assert P(2048, 8192, 4104)["variant"] == "TILE_2CTA_256x256"
     p = P(1024, 1024, 2048)
     # 16 pair tiles but a short K loop (32 blocks): 128x256 tiles in quarters
     assert p["variant"] == "TILE_1CTA_128x256" and p["k_split"] == 1
@@ -282,9 +289,10 @@ def test_plans_for_8bit_operands(lib):
     assert (p["num_full_tiles"], p["tail_split"]) == (988, 2)
     # A rows are half as large: up to 24 tile rows per 48 MiB group, 32 rows in 2 groups of 16
     assert p["group_m"] == 16
-    # 4112-byte rows: 33 K blocks, the last 16 wide; all of A (16 MiB) in one raster group
+    # 4112-byte rows are 16-byte units but not on 32-byte sectors: two
+    # consumers per CTA; 33 K blocks, the last 16 wide; all of A in one group
     p = P(4000, 11000, 4112)
-    assert p["variant"] == "TILE_2CTA_256x256" and p["k_blocks"] == 33 and p["group_m"] == 16
+    assert p["variant"] == "TILE_2CTA_512x256" and p["k_blocks"] == 33 and p["group_m"] == 8
     assert P(4000, 11000, 4128)["variant"] == "TILE_2CTA_256x256"
     with pytest.raises(g.GemmError):
         P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units

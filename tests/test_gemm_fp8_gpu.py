@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256,
-         g.Variant.TILE_2CTA_SPLITK]
+         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]
 DT = {"e4m3": g.Dtype.E4M3, "e5m2": g.Dtype.E5M2}
 
 
@@ -160,7 +160,7 @@ def test_fused_epilogue(fmt):
     A, B, sa, sb = inputs.operands_fp8(M, N, K, seed=33, fmt=fmt)
     C = inputs.draw_bf16(M, N, "uniform", 34)
     bias = inputs.draw_bf16(1, N, "uniform", 35).ravel()
-    for variant in [g.Variant.AUTO, g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_256x256]:
+    for variant in [g.Variant.AUTO, g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]:
         got = _run(A, B, fmt, variant, alpha=sa * 1.5, scale_n=sb, beta=-0.75, C=C, bias=bias, relu=True)
         want = _ref(A, B, fmt, sa * 1.5, sb, beta=-0.75, C=C, bias=bias, relu=True)
         check_close(got, want, K, f"epilogue {variant.name} {fmt}", dtype="bf16", scale=1.5)
@@ -179,7 +179,7 @@ def test_float8_tensors_and_uint8_agree():
 
 def test_deterministic_across_calls():
     A, B, sa, sb = inputs.operands_fp8(1024, 2048, 8192, seed=37, fmt="e4m3")
-    for variant in (g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_256x256, g.Variant.AUTO):
+    for variant in (g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256, g.Variant.AUTO):
         first = _run(A, B, "e4m3", variant, alpha=sa, scale_n=sb)
         assert np.array_equal(first, _run(A, B, "e4m3", variant, alpha=sa, scale_n=sb)), variant.name
     first = _run(A[:16], B, "e4m3", g.Variant.SKINNY_SPLITK, alpha=sa, scale_n=sb)

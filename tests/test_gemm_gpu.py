@@ -91,7 +91,7 @@ def test_named_workload_sampled(name):
 
 # ---------------------------------------------------------------- every variant, ragged
 TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256,
-         g.Variant.TILE_2CTA_SPLITK]
+         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]
 RAGGED = [(1, 8, 8), (7, 24, 40), (128, 128, 64), (129, 136, 72), (255, 264, 200),
           (300, 520, 1000), (513, 256, 4104), (640, 1000, 520)]
 SKINNY = [(1, 8, 8), (5, 136, 64), (16, 128, 64), (17, 200, 72), (33, 1000, 520),
@@ -271,3 +271,27 @@ def test_plan_on_device_matches_sm_count():
     assert 2 <= p["grid_ctas"] <= sms and p["grid_ctas"] % 2 == 0
     q = g.gemm_f16_nt_plan(16, 8192, 8192)
     assert q["grid_ctas"] == sms
+
+
+@pytest.mark.parametrize("shape", [(4000, 11000, 4104), (1000, 3000, 1000), (777, 520, 4104), (513, 1032, 64),
+                                   (1536, 2304, 1096)], ids=lambda s: "x".join(map(str, s)))
+def test_two_consumer_pairs(shape):
+    # two MMA consumers per CTA sharing each staged B tile (512 x 256 per pair):
+    # ragged M (a second consumer on rows past M), ragged N and K, column
+    # pieces in the last round, several rounds on the single-buffered
+    # accumulators; consecutive calls give the same bits
+    M, N, K = shape
+    plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.TILE_2CTA_512x256)
+    assert plan["variant"] == "TILE_2CTA_512x256" and plan["tile_m"] == 512 and plan["grid_ctas"] % 2 == 0
+    A, B = inputs.operands(M, N, K, seed=5000 + M + N + K)
+    if M * N * K <= 2e10:
+        _full_parity(A, B, g.Variant.TILE_2CTA_512x256)
+        d1 = _run(A, B, g.Variant.TILE_2CTA_512x256)
+        d2 = _run(A, B, g.Variant.TILE_2CTA_512x256)
+        assert np.array_equal(d1.view(np.uint16), d2.view(np.uint16)), "two-consumer result differs between calls"
+    else:
+        d = _run(A, B, g.Variant.TILE_2CTA_512x256)
+        rows, cols = inputs.sample_entries(M, N, seed=11, extra_rows=_edge_indices(M, 256),
+                                           extra_cols=_edge_indices(N, 256))
+        check_close(d[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "two-consumer sampled")
+        assert not np.any(np.isnan(d))
