@@ -190,6 +190,25 @@ __device__ __forceinline__ float epi_apply1(const EpiParams& e, float x, int64_t
     return x;
 }
 
+// The per-column part of the transform for one output column n (alpha *
+// s[n] and the bias), fetched ahead of use; apply() is epi_apply1 with them.
+template <class T>
+struct EpiColumnFactors {
+    float a = 1.0f;   // alpha * s[n]
+    float b = 0.0f;   // bias[n]
+    __device__ __forceinline__ void load(const EpiParams& e, int64_t n) {
+        a = e.scale_n != nullptr ? e.alpha * e.scale_n[n] : e.alpha;
+        b = e.bias != nullptr ? Elem<T>::to_float(static_cast<const T*>(e.bias)[n]) : 0.0f;
+    }
+    __device__ __forceinline__ float apply(const EpiParams& e, float x, int64_t row, int64_t col, int64_t N) const {
+        x *= a;
+        if (e.C != nullptr && e.beta != 0.0f) x += e.beta * Elem<T>::to_float(static_cast<const T*>(e.C)[row * N + col]);
+        if (e.bias != nullptr) x += b;
+        if (e.act == 1) x = x < 0.0f ? 0.0f : x;
+        return x;
+    }
+};
+
 // One output column n of the small-M kernel (rows 0..MN-1): the C values and
 // the bias are fetched with independent loads before any output is written,
 // so their latencies overlap (and an in-place C == D is read before it is

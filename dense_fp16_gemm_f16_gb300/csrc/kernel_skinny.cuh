@@ -203,6 +203,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int64_t r = cid; r < p.ranges; r += C, ++it) {
                 const uint32_t buf = it & 1u;
                 const uint32_t use = (it >> 1) & 1u;
+                const int64_t n = r * p.width + n_local;
+                const bool col_in = n_local < p.width && n < p.N;
+                // this column's C values, factor and bias, fetched while the K loop runs
+                EpiColumn<T, MN> ec;
+                if (p.epi.on && col_in) ec.load(p.epi, n, p.M, p.N);
                 if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) break;
                 ptx::tc_fence_after();
                 uint32_t v[MN];
@@ -211,11 +216,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
-                const int64_t n = r * p.width + n_local;
-                if (n_local < p.width && n < p.N) {
+                if (col_in) {
                     if (p.epi.on) {
-                        EpiColumn<T, MN> ec;
-                        ec.load(p.epi, n, p.M, p.N);
 #pragma unroll
                         for (int m = 0; m < MN; ++m)
                             if (m < p.M)
@@ -232,6 +234,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // One range per cluster (the planner launches exactly R clusters).
             // Every thread reaches the exchange barrier, whatever happened before.
             const int64_t r = cid;
+            const int64_t n = r * p.width + n_local;
+            const bool col_in = r < p.ranges && n_local < p.width && n < p.N;
+            // this column's factor alpha * s[n] and bias, fetched while the K loop runs
+            EpiColumnFactors<T> cf;
+            if (p.epi.on && col_in) cf.load(p.epi, n);
             const bool ready = r < p.ranges &&
                                wait_phase_warp(tfull_bar(0), 0, p.status, kSiteEpilogueTmemFull, p.timeout_ns);
             uint32_t v[MN];
@@ -257,14 +264,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
             ptx::cluster_sync();   // exchange barrier: every partial of this CTA's rows is in
             const float* rv = reinterpret_cast<const float*>(smem + Cfg::OFF_RECV);
-            const int64_t n = r * p.width + n_local;
-            if (ready && n_local < p.width && n < p.N) {
+            if (ready && col_in) {
                 for (int ml = 0; ml < MS; ++ml) {
                     const int m = j * MS + ml;
                     if (m >= p.M) break;
                     float acc = 0.0f;
                     for (int i = 0; i < P; ++i) acc += rv[(i * MS + ml) * 128 + n_local];   // ascending pieces
-                    const float x = p.epi.on ? epi_apply1<T>(p.epi, acc, m, n, p.N) : acc;
+                    const float x = p.epi.on ? cf.apply(p.epi, acc, m, n, p.N) : acc;
                     D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
                 }
             }
