@@ -178,17 +178,21 @@ Limits host_limits(int sms) {
 // and R must reach ceil(N / 128) (ranges of at most 128 columns); with P = 1
 // ranges are dealt to at most one CTA per SM, in as many rounds as needed.
 // Each choice is timed with a simple model and the fastest wins (ties keep
-// the smaller P).  A CTA runs rounds * ceil(kb / P) ring stages and moves
-// (width + M) rows of 128 bytes per stage (its B rows and A's M rows); it
-// takes the longer of those bytes at its share of HBM bandwidth and its
-// stages at one per kSkinnyStageUs, plus the in-cluster sum when P > 1.
-// Measured on GB300 (all P forced in turn): a CTA finishes at most about one
-// stage per 0.25 us however narrow its B slot (the four MMAs of a stage and
-// their barrier round trip), so narrow ranges are stage-bound and lose to
-// wider ones split over a cluster -- e.g. 1 x 8192 x 8192: 152 ranges of 54
-// columns 31.4 us, 76 ranges of 108 columns in pairs 21.6 us.
+// the smaller P).  A CTA runs rounds * ceil(kb / P) K blocks of (width + M)
+// rows of 128 bytes (its B rows and A's M rows), in ring stages of
+// skinny_stage_atoms() blocks; it takes the longer of those bytes at its share
+// of HBM bandwidth and of its issue time (kSkinnyStageUs per stage plus
+// kSkinnyAtomUs per K block), plus a quarter of the shorter one (the two
+// never overlap perfectly), plus the in-cluster sum when P > 1.  The issue
+// costs are measured on GB300 with P forced (builds fixing P) and the blocks
+// per stage varied: 16 x 1024 x 8192 on 152 ranges of 7 columns (P = 1) takes
+// 35.8 / 24.5 / 20.2 us with 1 / 2 / 4 K blocks per stage, 0.28 / 0.38 /
+// 0.63 us per stage whatever the bytes.  At N = 8192 ranges of 108 columns in
+// pairs beat 152 ranges of 54 by 0.5-2.4 us (fp16 and E4M3, M = 1-64).
 constexpr double kSkinnyHbmBytesPerUs = 6.7e6;
-constexpr double kSkinnyStageUs = 0.25;
+constexpr double kSkinnyOverlapLoss = 0.25;
+constexpr double kSkinnyStageUs = 0.18;
+constexpr double kSkinnyAtomUs = 0.10;
 constexpr double kSkinnyExchangeUs = 0.5;
 
 struct SkinnyShape {
@@ -196,7 +200,12 @@ struct SkinnyShape {
     int64_t ranges, width, rounds, grid;
 };
 
-SkinnyShape plan_skinny(int64_t M, int64_t N, int64_t kb, const Limits& lim) {
+// K blocks the small-M ring holds for ranges of `width` columns.
+int skinny_ring_atoms(const SkinnyOps& ops, int64_t width) {
+    return std::min(ops.max_atoms, ops.ring_bytes / (skinny_w_stride(static_cast<int>(width)) + ops.x_bytes));
+}
+
+SkinnyShape plan_skinny(int64_t M, int64_t N, int64_t kb, const Limits& lim, const SkinnyOps& ops) {
     const int64_t G = lim.sms;
     const int64_t r_min = cdiv(N, 128);
     SkinnyShape best{1, 0, 0, 0, 0};
@@ -219,9 +228,14 @@ SkinnyShape plan_skinny(int64_t M, int64_t N, int64_t kb, const Limits& lim) {
             sh.grid = sh.ranges * pc;
         }
         sh.width = cdiv(N, sh.ranges);
-        const double stages = static_cast<double>(sh.rounds * cdiv(kb, pc));
-        const double bytes = stages * static_cast<double>((sh.width + M) * kStageRowBytes);
-        double t = std::max(bytes * static_cast<double>(sh.grid) / kSkinnyHbmBytesPerUs, stages * kSkinnyStageUs) +
+        const int64_t per_range = cdiv(kb, pc);
+        const int64_t ka = skinny_stage_atoms(skinny_ring_atoms(ops, sh.width));
+        const double atoms = static_cast<double>(sh.rounds * per_range);
+        const double stages = static_cast<double>(sh.rounds * cdiv(per_range, ka));
+        const double bytes = atoms * static_cast<double>((sh.width + M) * kStageRowBytes);
+        const double t_bytes = bytes * static_cast<double>(sh.grid) / kSkinnyHbmBytesPerUs;
+        const double t_issue = stages * kSkinnyStageUs + atoms * kSkinnyAtomUs;
+        double t = std::max(t_bytes, t_issue) + kSkinnyOverlapLoss * std::min(t_bytes, t_issue) +
                    (pc > 1 ? kSkinnyExchangeUs : 0.0);
 #ifdef GEMM_SKINNY_PIECES
         if (pc == GEMM_SKINNY_PIECES) t = -1.0;
@@ -232,6 +246,27 @@ SkinnyShape plan_skinny(int64_t M, int64_t N, int64_t kb, const Limits& lim) {
         }
     }
     return best;
+}
+
+// B blocks (width rows of 128 bytes) each small-M CTA prefetches into L2
+// before its dependency wait, while the previous kernel in the stream
+// finishes: the whole grid prefetches at most kSkinnyPrefetchPct percent of
+// B and at most kSkinnyPrefetchBytes (at least one block per CTA).
+#ifndef GEMM_SKINNY_PREFETCH_MB
+#define GEMM_SKINNY_PREFETCH_MB 48
+#endif
+#ifndef GEMM_SKINNY_PREFETCH_PCT
+#define GEMM_SKINNY_PREFETCH_PCT 50
+#endif
+constexpr int64_t kSkinnyPrefetchBytes = int64_t{GEMM_SKINNY_PREFETCH_MB} << 20;
+constexpr int64_t kSkinnyPrefetchPct = GEMM_SKINNY_PREFETCH_PCT;
+
+int32_t skinny_prefetch_blocks(const gemm_plan_t& pl, int64_t b_bytes) {
+    const int64_t per_block = static_cast<int64_t>(pl.grid_ctas) * pl.tile_n * kStageRowBytes;
+    const int64_t piece = cdiv(pl.k_blocks, pl.k_split);
+    const int64_t budget = std::min<int64_t>(kSkinnyPrefetchBytes, b_bytes / 100 * kSkinnyPrefetchPct);
+    const int64_t n = per_block > 0 ? budget / per_block : 1;
+    return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(n, piece)));
 }
 
 int skinny_mn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
@@ -297,17 +332,17 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
         const SkinnyOps& ops = skinny_ops(mn, 0);
         pl->cta_group = 1;
         pl->tile_m = mn;
-        pl->stages = std::min(ops.max_stages, ops.ring_bytes / (skinny_w_stride(128) + ops.x_bytes));
+        pl->stages = skinny_ring_atoms(ops, 128);
         pl->smem_bytes = ops.smem_bytes;
         pl->tmem_cols = ops.tmem_cols;
         pl->m_tiles = 1;
         pl->tile_n = 128;
         pl->n_tiles = cdiv(N, 128);
         if (M == 0 || N == 0 || K == 0) return GEMM_OK;
-        const SkinnyShape sh = plan_skinny(M, N, pl->k_blocks, lim);
+        const SkinnyShape sh = plan_skinny(M, N, pl->k_blocks, lim, ops);
         pl->tile_n = static_cast<int32_t>(sh.width);
-        // ring stages of B slots sized to the range width (narrow ranges get more)
-        pl->stages = std::min(ops.max_stages, ops.ring_bytes / (skinny_w_stride(pl->tile_n) + ops.x_bytes));
+        // K blocks in flight: B slots sized to the range width (narrow ranges get more)
+        pl->stages = skinny_ring_atoms(ops, pl->tile_n);
         pl->n_tiles = sh.ranges;
         pl->k_split = sh.pieces;
         pl->grid_ctas = static_cast<int32_t>(sh.grid);
@@ -677,7 +712,8 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         p.width = pl.tile_n;
         p.ranges = static_cast<int32_t>(pl.n_tiles);
         p.pieces = pl.k_split;
-        p.stages = pl.stages;
+        p.stage_atoms = skinny_stage_atoms(pl.stages);
+        p.stages = pl.stages / p.stage_atoms;
         p.w_stride = skinny_w_stride(pl.tile_n);
         p.D = D;
         p.epi = epi;
@@ -685,6 +721,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
         p.timeout_ns = timeout_for(pl.k_blocks);
         p.stream_b = b_bytes >= kStreamBBytes ? 1 : 0;
         p.ab_format = dtype_ab_format(dtype);
+        p.prefetch_blocks = skinny_prefetch_blocks(pl, b_bytes);
         if (ops.launch(tw, tx, p, pl.grid_ctas, s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;

@@ -239,6 +239,17 @@ inline int choose_ksplit(int64_t tiles, const int* clusters, int64_t k_blocks) {
 // range's B rows, and the P fp32 partials are summed inside the cluster
 // through distributed shared memory.  With P = 1 a CTA may own several
 // ranges (persistent, one after the other).
+// Independent accumulators per output block of the small-M kernel.  Its MMAs
+// are narrow (N = MN <= 64), so one MMA adds into an accumulator in much less
+// time than the next MMA on the same accumulator has to wait for it; with the
+// four MMAs of a ring stage on four different accumulators they overlap, and
+// the epilogue adds the four in a fixed order.
+#ifndef GEMM_SKINNY_ACCS
+#define GEMM_SKINNY_ACCS 4
+#endif
+constexpr int kSkinnyAccs = GEMM_SKINNY_ACCS;
+static_assert(kSkinnyAccs == 1 || kSkinnyAccs == 2 || kSkinnyAccs == 4, "accumulators per block: 1, 2 or 4");
+
 template <int MN_>
 struct SkinnyConfig {
     static constexpr int MN = MN_;
@@ -249,11 +260,16 @@ struct SkinnyConfig {
     // slot's base: past a narrow slot it reads the next slot (or, for the last
     // one, the A slots and buffers behind the ring, all inside this CTA's
     // shared memory); those rows only feed TMEM lanes that are never used.
-    static constexpr int MAX_STAGES = 32;
-    // partials received from the cluster: [P][MN / P][128] fp32 = MN * 128 fp32
+    static constexpr int MAX_STAGES = 32;   // ring stages (barrier pairs)
+    static constexpr int MAX_ATOMS = 64;    // K blocks in flight (a stage holds one or more)
+    // partials received from the cluster: [P][128 columns][MN / P rows] fp32 = MN * 128 fp32
     static constexpr int RECV_BYTES = MN * 128 * 4;
     static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
-    static constexpr int TMEM_COLS = (2 * MN < 32) ? 32 : 2 * MN;
+    // Each accumulator buffer is kSkinnyAccs independent MN-column
+    // accumulators (MMA k of a stage adds into accumulator k % kSkinnyAccs),
+    // two buffers.
+    static constexpr int ACC_COLS = kSkinnyAccs * MN;
+    static constexpr int TMEM_COLS = (2 * ACC_COLS < 32) ? 32 : 2 * ACC_COLS;
     // ring = [stages B slots][stages A slots], split at run time (ring_stages)
     static constexpr int RING_BYTES = (kMaxDynSmem - 1024 - RECV_BYTES - NUM_BARS * 8 - 16) / 1024 * 1024;
     static constexpr int OFF_RECV = RING_BYTES;
@@ -261,15 +277,27 @@ struct SkinnyConfig {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
     static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
+    static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
     static_assert(RING_BYTES / (128 * kStageRowBytes + X_BYTES) >= 4, "at least four full-width stages");
     static_assert(RECV_BYTES + NUM_BARS * 8 >= 0, "layout");
     static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");
 };
 
-// Stride of a B slot for ranges of `width` columns; a launch's ring has
-// min(MAX_STAGES, RING_BYTES / (stride + X_BYTES)) stages.
+// Stride of a B slot for ranges of `width` columns; a launch's ring holds
+// min(MAX_ATOMS, RING_BYTES / (stride + X_BYTES)) K blocks, grouped into
+// stages of skinny_stage_atoms() blocks.
 GEMM_HD int skinny_w_stride(int width) { return (width * kStageRowBytes + 1023) / 1024 * 1024; }
+
+// K blocks per ring stage for a ring of `atoms` K blocks: as many as leave at
+// least three stages, at most 8.  Every stage costs a fixed ~0.18 us (its
+// barrier round trip), each K block in it ~0.1 us more (its copies and four
+// MMAs), so narrow ranges and 8-bit operands, whose K blocks are few bytes,
+// need several per stage to keep up with HBM.
+GEMM_HD int skinny_stage_atoms(int atoms) {
+    const int a = atoms / 3;
+    return a < 1 ? 1 : (a > 8 ? 8 : a);
+}
 
 using CfgSkinny16 = SkinnyConfig<16>;
 using CfgSkinny32 = SkinnyConfig<32>;
@@ -284,7 +312,8 @@ struct SkinnyParams {
     int32_t width;            // columns per range (rows of a B box), 1..128
     int32_t ranges;           // R; range r covers columns [r * width, r * width + width) (clipped at N)
     int32_t pieces;           // P = CTAs per cluster; CTA j runs K blocks [j kb / P, (j + 1) kb / P)
-    int32_t stages;           // ring stages, each a B slot of w_stride bytes and an A slot
+    int32_t stages;           // ring stages, each stage_atoms B slots of w_stride bytes and as many A slots
+    int32_t stage_atoms;      // K blocks (128-byte atoms of K) per ring stage
     int32_t w_stride;         // skinny_w_stride(width)
     void* D;                  // fp16 or bf16 [M][N]
     EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)
@@ -292,6 +321,7 @@ struct SkinnyParams {
     uint64_t timeout_ns;
     int32_t stream_b;         // B is too large to stay in L2: load it evict-first
     uint32_t ab_format;       // operand format field of the MMA instruction descriptor
+    int32_t prefetch_blocks;  // B blocks a CTA prefetches into L2 before its dependency wait
 };
 
 // Stream-K kernel (GEMM_VARIANT_SKINNY_STREAMK, and the no-allocation entry
@@ -315,6 +345,7 @@ struct StreamKConfig {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
     static_assert(X_BYTES % 1024 == 0, "activation tile must stay 1024-aligned");
+    static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert(MN == 16 || MN == 32 || MN == 64, "narrow side must be 16, 32 or 64");
     static_assert(SMEM_BYTES <= kMaxDynSmem, "shared memory budget exceeded");

@@ -39,6 +39,22 @@
 
 namespace gemm_gb300 {
 
+// The output block held in TMEM at `taddr` (this warp's lanes): the sum of
+// its kSkinnyAccs accumulators, added in ascending order.
+template <int MN>
+__device__ __forceinline__ void skinny_acc_sum(uint32_t taddr, uint32_t (&v)[MN]) {
+    ptx::tmem_ld_cols<MN>(taddr, v);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int a = 1; a < kSkinnyAccs; ++a) {
+        uint32_t w[MN];
+        ptx::tmem_ld_cols<MN>(taddr + static_cast<uint32_t>(a * MN), w);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < MN; ++m) v[m] = __float_as_uint(__uint_as_float(v[m]) + __uint_as_float(w[m]));
+    }
+}
+
 // T is the element type of D (and C, bias); F8 selects 8-bit operands.
 template <class Cfg, class T, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -61,10 +77,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * MAXS + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * MAXS + 4);
     const uint32_t slot = sbase + Cfg::OFF_SLOT;
-    // ring of this launch: `stages` B slots of w_stride bytes, then as many A slots
+    // ring of this launch: `stages` stages of KA K blocks each; a stage's B
+    // slots (w_stride bytes per K block) first, the A slots after all of them
     const int STAGES = p.stages;
-    auto w_slot = [&](int s) { return sbase + static_cast<uint32_t>(s * p.w_stride); };
-    auto x_slot = [&](int s) { return sbase + static_cast<uint32_t>(STAGES * p.w_stride + s * Cfg::X_BYTES); };
+    const int KA = p.stage_atoms;
+    auto w_slot = [&](int s, int a) { return sbase + static_cast<uint32_t>((s * KA + a) * p.w_stride); };
+    auto x_slot = [&](int s, int a) {
+        return sbase + static_cast<uint32_t>(STAGES * KA * p.w_stride + (s * KA + a) * Cfg::X_BYTES);
+    };
     // K pieces per range = CTAs per cluster (the same for the whole grid)
     const int P = p.pieces;
     const bool clustered = P > 1;
@@ -103,7 +123,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // blocks of this CTA's first ring fill into L2 (a prefetch cannot expose
     // stale data, so it may run before the dependency wait below).
     if (warp == 0 && lane == 0 && cid < p.ranges) {
-        const int n_pre = (kb1 - kb0) < STAGES ? (kb1 - kb0) : STAGES;
+        const int n_pre = (kb1 - kb0) < p.prefetch_blocks ? (kb1 - kb0) : p.prefetch_blocks;
         for (int i = 0; i < n_pre; ++i)
             ptx::tma_prefetch_2d(&tmW, (kb0 + i) * kStageK, static_cast<int32_t>(cid * p.width));
     }
@@ -128,15 +148,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const uint32_t stage_bytes = static_cast<uint32_t>(p.width) * kStageRowBytes + Cfg::X_BYTES;
         for (int64_t r = cid; ok && r < p.ranges; r += C) {
             const int32_t y = static_cast<int32_t>(r * p.width);
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int kb = kb0; kb < kb1; kb += KA) {
+                const int na = (kb1 - kb) < KA ? (kb1 - kb) : KA;
                 if (!wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 if (ptx::elect_one()) {
-                    ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-                    ptx::tma_load_2d_hint(w_slot(stage), &tmW, full_bar(stage), kb * kStageK, y, pol_w);
-                    ptx::tma_load_2d_hint(x_slot(stage), &tmX, full_bar(stage), kb * kStageK, 0, pol_x);
+                    ptx::mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(na) * stage_bytes);
+                    for (int a = 0; a < na; ++a) {
+                        ptx::tma_load_2d_hint(w_slot(stage, a), &tmW, full_bar(stage), (kb + a) * kStageK, y, pol_w);
+                        ptx::tma_load_2d_hint(x_slot(stage, a), &tmX, full_bar(stage), (kb + a) * kStageK, 0, pol_x);
+                    }
                 }
                 __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -164,20 +187,24 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t d_tmem = tmem_base + buf * MN;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
+            for (int kb = kb0; kb < kb1; kb += KA) {
+                const int na = (kb1 - kb) < KA ? (kb1 - kb) : KA;
                 if (!wait_phase_warp(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint64_t w_desc = ptx::sw128_kmajor_desc(w_slot(stage));
-                const uint64_t x_desc = ptx::sw128_kmajor_desc(x_slot(stage));
                 if (ptx::elect_one()) {
+                    for (int a = 0; a < na; ++a) {
+                        const uint64_t w_desc = ptx::sw128_kmajor_desc(w_slot(stage, a));
+                        const uint64_t x_desc = ptx::sw128_kmajor_desc(x_slot(stage, a));
 #pragma unroll
-                    for (int k = 0; k < kMmaPerStage; ++k)
-                        ptx::mma<1, F8>(d_tmem, w_desc + 2u * k, x_desc + 2u * k, idesc,
-                                        (kb != kb0 || k != 0) ? 1u : 0u);
+                        for (int k = 0; k < kMmaPerStage; ++k)
+                            ptx::mma<1, F8>(d_tmem + static_cast<uint32_t>((k % kSkinnyAccs) * MN), w_desc + 2u * k,
+                                            x_desc + 2u * k, idesc,
+                                            (kb != kb0 || a != 0 || k >= kSkinnyAccs) ? 1u : 0u);
+                    }
                     ptx::mma_commit(empty_bar(stage));
                 }
                 __syncwarp();
@@ -211,8 +238,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) break;
                 ptx::tc_fence_after();
                 uint32_t v[MN];
-                ptx::tmem_ld_cols<MN>(t_lane + buf * MN, v);
-                ptx::tmem_wait_ld();
+                skinny_acc_sum<MN>(t_lane + buf * Cfg::ACC_COLS, v);
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
@@ -244,34 +270,70 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint32_t v[MN];
             if (ready) {
                 ptx::tc_fence_after();
-                ptx::tmem_ld_cols<MN>(t_lane, v);
-                ptx::tmem_wait_ld();
+                skinny_acc_sum<MN>(t_lane, v);
             } else {
 #pragma unroll
                 for (int m = 0; m < MN; ++m) v[m] = 0u;
             }
-            // CTA d finishes rows [d MS, (d+1) MS) (MS = MN / P, P a power of two);
-            // its receive buffer is [P pieces][MS rows][128 columns] fp32
+            // CTA d finishes rows [d MS, (d+1) MS) (MS = MN / P, P a power of two).
+            // Its receive buffer is [P pieces][128 columns][MS rows] fp32: a
+            // column's rows bound for one CTA are contiguous, so they travel as
+            // 16-byte stores (8-byte when MS = 2), a quarter of the remote
+            // transactions of one store per value.
             const int ms_shift = (__ffs(MN) - 1) - (__ffs(P) - 1);
             const int MS = 1 << ms_shift;
             const uint32_t recv = sbase + Cfg::OFF_RECV;
+            const uint32_t mine = recv + static_cast<uint32_t>((j * 128 + n_local) * MS * 4);
+            if (MS >= 4) {
 #pragma unroll
-            for (int m = 0; m < MN; ++m) {
-                const int d = m >> ms_shift;
-                const int ml = m - (d << ms_shift);
-                const uint32_t off = static_cast<uint32_t>(((j * MS + ml) * 128 + n_local) * 4);
-                ptx::st_cluster_f32(ptx::mapa(recv + off, static_cast<uint32_t>(d)), __uint_as_float(v[m]));
+                for (int m = 0; m < MN; m += 4) {
+                    const int d = m >> ms_shift;
+                    const uint32_t off = static_cast<uint32_t>((m - (d << ms_shift)) * 4);
+                    ptx::st_cluster_v4(ptx::mapa(mine + off, static_cast<uint32_t>(d)), v[m], v[m + 1], v[m + 2], v[m + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < MN; m += 2) {
+                    const int d = m >> ms_shift;
+                    const uint32_t off = static_cast<uint32_t>((m - (d << ms_shift)) * 4);
+                    ptx::st_cluster_v2(ptx::mapa(mine + off, static_cast<uint32_t>(d)), v[m], v[m + 1]);
+                }
             }
             ptx::cluster_sync();   // exchange barrier: every partial of this CTA's rows is in
-            const float* rv = reinterpret_cast<const float*>(smem + Cfg::OFF_RECV);
             if (ready && col_in) {
-                for (int ml = 0; ml < MS; ++ml) {
+                // this column's rows [j MS, (j+1) MS), the P partials added in
+                // ascending piece order
+                const uint32_t col = recv + static_cast<uint32_t>(n_local * MS * 4);
+                const uint32_t piece_bytes = static_cast<uint32_t>(128 * MS * 4);
+                auto finish = [&](int ml, float acc) {
                     const int m = j * MS + ml;
-                    if (m >= p.M) break;
-                    float acc = 0.0f;
-                    for (int i = 0; i < P; ++i) acc += rv[(i * MS + ml) * 128 + n_local];   // ascending pieces
-                    const float x = p.epi.on ? cf.apply(p.epi, acc, m, n, p.N) : acc;
-                    D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
+                    if (m < p.M) {
+                        const float x = p.epi.on ? cf.apply(p.epi, acc, m, n, p.N) : acc;
+                        D[m * static_cast<int64_t>(p.N) + n] = Elem<T>::from_float(x);
+                    }
+                };
+                if (MS >= 4) {
+                    for (int c = 0; c < MS; c += 4) {
+                        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        for (int i = 0; i < P; ++i) {
+                            float t[4];
+                            ptx::ld_shared_v4(col + i * piece_bytes + static_cast<uint32_t>(c * 4), t);
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) acc[r] += t[r];
+                        }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) finish(c + r, acc[r]);
+                    }
+                } else {
+                    float acc[2] = {0.0f, 0.0f};
+                    for (int i = 0; i < P; ++i) {
+                        float t[2];
+                        ptx::ld_shared_v2(col + i * piece_bytes, t);
+                        acc[0] += t[0];
+                        acc[1] += t[1];
+                    }
+                    finish(0, acc[0]);
+                    finish(1, acc[1]);
                 }
             }
         }

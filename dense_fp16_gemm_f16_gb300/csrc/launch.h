@@ -27,8 +27,8 @@ struct TiledOps {
 };
 
 struct SkinnyOps {
-    // the ring a launch divides into min(max_stages, ring_bytes / (B slot + x_bytes)) stages
-    int mn, ring_bytes, x_bytes, max_stages, smem_bytes, tmem_cols;
+    // the ring holds min(max_atoms, ring_bytes / (B slot + x_bytes)) K blocks
+    int mn, ring_bytes, x_bytes, max_atoms, smem_bytes, tmem_cols;
     cudaError_t (*prepare)();
     // co-resident clusters of `pieces` CTAs on the current device
     cudaError_t (*max_active)(int pieces, int* out);

@@ -99,6 +99,21 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr_cluster, uint32_t a,
                  :: "r"(addr_cluster), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 8-byte store (two 32-bit words) to shared memory given by its
+// shared::cluster address.
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr_cluster, uint32_t a, uint32_t b) {
+    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" :: "r"(addr_cluster), "r"(a), "r"(b) : "memory");
+}
+
+// 16-byte and 8-byte loads from this CTA's shared memory (shared::cta address).
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ld_shared_v2(uint32_t addr, float (&v)[2]) {
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(addr) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");

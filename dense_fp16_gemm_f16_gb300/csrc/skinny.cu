@@ -50,7 +50,7 @@ struct SkinnyLauncher {
         return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<Cfg, T, F8>, w, x, p);
     }
     static const SkinnyOps& ops() {
-        static const SkinnyOps o = {Cfg::MN,         Cfg::RING_BYTES, Cfg::X_BYTES, Cfg::MAX_STAGES,
+        static const SkinnyOps o = {Cfg::MN,         Cfg::RING_BYTES, Cfg::X_BYTES, Cfg::MAX_ATOMS,
                                     Cfg::SMEM_BYTES, Cfg::TMEM_COLS,  &prepare,     &max_active,
                                     &launch};
         return o;

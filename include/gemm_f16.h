@@ -239,7 +239,8 @@ typedef struct {
     int32_t tile_m;          /* output rows per tile (per CTA pair when cta_group == 2) */
     int32_t tile_n;          /* output columns per tile */
     int32_t tile_k;          /* K elements per pipeline stage */
-    int32_t stages;          /* shared-memory pipeline depth */
+    int32_t stages;          /* shared-memory pipeline depth in K blocks (the column-range
+                                small-M kernel groups them into ring stages of up to 8) */
     int64_t m_tiles, n_tiles;/* tile grid (small M: m_tiles = 1; n_tiles = column ranges of
                                 tile_n columns, or tiles of 128 for the stream-K kernel) */
     int64_t k_blocks;        /* ceil(K / tile_k) */
@@ -248,8 +249,8 @@ typedef struct {
     int32_t tmem_cols;       /* TMEM columns allocated per CTA */
     int32_t max_tiles_per_cta; /* small M: column ranges per CTA (stream-K: partial-sum
                                   slots per CTA), else 0 */
-    int64_t workspace_bytes; /* fp32 partials + counters of the stream-K and tiled
-                                split-K kernels, else 0 */
+    int64_t workspace_bytes; /* fp32 partials + counters of the stream-K small-M kernel,
+                                else 0 */
     int64_t num_full_tiles;  /* tiled: tiles run whole (the persistent grid's full rounds) */
     int32_t tail_split;      /* tiled: the other tiles are cut into this many column pieces */
     int32_t group_m;         /* tiled: tile rows per raster group (L2 reuse of A) */

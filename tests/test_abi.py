@@ -227,7 +227,9 @@ def test_skinny_ranges_and_pieces(lib):
     # very short K: every CTA one range of 14 columns, no split
     p = P(7, 2048, 192)
     assert (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (1, 152, 14, 152)
-    assert p["stages"] == 32     # narrow B slots: the ring holds its most stages
+    # narrow B slots: the ring holds 54 K blocks in flight (1 KB of B and 2 KB of A
+    # each), launched as stages of 8 blocks
+    assert p["stages"] == 54
     # few columns, long K: clusters of 8 pieces, 19 ranges of 54 columns
     p = P(16, 1024, 8192)
     assert (p["k_split"], p["n_tiles"], p["tile_n"], p["grid_ctas"]) == (8, 19, 54, 152)
