@@ -271,6 +271,20 @@ int32_t skinny_prefetch_blocks(const gemm_plan_t& pl, int64_t b_bytes) {
 
 int skinny_mn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// K blocks per ring stage of the tiled kernel.  A launch made only of column
+// pieces (narrow MMAs: a stage's MMAs take less time than the stage's barrier
+// round trip) takes two K blocks per stage where the configuration has that
+// form (the 1-CTA ones); otherwise one.  Measured on GB300
+// (fp16, back to back): 1024 x 1024 x 2048 on 128 pieces of 128 x 64, 13.2 ->
+// 10.8 us with two; whole 128 x 256 tiles at 2048^3 15.97 -> 17.05 us and pair
+// tiles 1-4 % slower with two.
+int32_t tiled_stage_atoms(const gemm_plan_t& pl, int max_atoms) {
+    int32_t a = (pl.num_full_tiles == 0 && pl.tail_split > 1 && pl.k_split == 1) ? 2 : 1;
+    if (a > max_atoms) a = max_atoms;
+    while (a > 1 && pl.stages / a < 2) --a;
+    return a;
+}
+
 // The ops table of a tiled variant.
 const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
     switch (v) {
@@ -793,6 +807,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
     p.last_k_steps = static_cast<int32_t>(cdiv(K * in_bytes - (pl.k_blocks - 1) * kStageRowBytes, 32));
     p.num_units = pl.k_split > 1 ? p.num_tiles
                                  : pl.num_full_tiles + (p.num_tiles - pl.num_full_tiles) * pl.tail_split;
+    p.stage_atoms = tiled_stage_atoms(pl, ops.max_stage_atoms);
     p.D = D;
     p.epi = epi;
     p.status = dev->status;

@@ -124,6 +124,7 @@ struct TiledParams {
                               // ksplit MMA groups of one cluster (split K)
     uint32_t ab_format;       // operand format field of the MMA instruction descriptor
     int32_t last_k_steps;     // 32-byte K steps of real data in the last K block (1..4)
+    int32_t stage_atoms;      // K blocks per ring stage (consecutive ring slots)
     void* D;                  // the output (fp16 or bf16 [M][N]); written directly by the
                               // split-K slice sums, through tmD otherwise
     EpiParams epi;            // fused output transform (epi.on == 0: plain D = A B^T)

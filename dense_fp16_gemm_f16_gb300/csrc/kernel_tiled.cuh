@@ -141,8 +141,10 @@ __device__ __forceinline__ void split_k_reduce(const uint8_t* recv, const TiledP
 }
 
 // T is the element type of D (and C, bias); F8 selects 8-bit operands
-// (kind::f8f6f4, 128 K elements per stage) instead of 16-bit ones of type T.
-template <class Cfg, class T, bool F8>
+// (kind::f8f6f4, 128 K elements per stage) instead of 16-bit ones of type T;
+// KA = K blocks per ring stage (a compile-time constant, so the one-block
+// loops compile to straight-line issue code).
+template <class Cfg, class T, bool F8, int KA = 1>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
 gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBpiece, const __grid_constant__ CUtensorMap tmD,
@@ -180,8 +182,11 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * MAXS + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * MAXS + 4);
     // ring geometry of this launch (the same in every role and both CTAs of a pair)
+    // ring of this launch: slots of `stride` bytes (one K block of A and B),
+    // grouped into STAGES stages of KA consecutive slots
     const uint32_t stride = static_cast<uint32_t>(ring_stride(p, Cfg::A_BYTES, Cfg::B_BYTES));
-    const int STAGES = static_cast<int>(Cfg::RING_BYTES / stride);
+    const int STAGES = static_cast<int>(Cfg::RING_BYTES / stride) / KA;
+    auto slot_addr = [&](int s, int a) { return sbase + static_cast<uint32_t>(s * KA + a) * stride; };
     const uint32_t slot = sbase + Cfg::OFF_SLOT;
 
     if (warp == 0 && lane == 0) {
@@ -245,33 +250,37 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const bool piece = nw < Cfg::BN;
                 const CUtensorMap* b_map = piece ? &tmBpiece : &tmB;
                 const uint32_t stage_bytes = Cfg::A_BYTES + (piece ? Cfg::B_BYTES / p.split : Cfg::B_BYTES);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += KA) {
+                    const int na = (KA == 1 || kb1 - kb >= KA) ? KA : kb1 - kb;
                     if (!wait_phase_warp(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty,
                                          p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a_dst = sbase + stage * stride;
-                    const uint32_t b_dst = a_dst + Cfg::A_BYTES;
-                    const int kx = (reverse ? (kb1 - 1 - (kb - kb0)) : kb) * kStageK;
                     if (ptx::elect_one()) {
-                        if constexpr (CG == 1) {
-                            ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+                        // Both CTAs' bytes of a pair complete on the leader's full
+                        // barrier; the leader announces the pair's total.
+                        const uint32_t bar = CG == 1 ? full_bar(stage) : ptx::mapa(full_bar(stage), leader);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), CG * na * stage_bytes);
 #pragma unroll
-                            for (int h = 0; h < CONS; ++h)
-                                ptx::tma_load_2d(a_dst + h * Cfg::A_HALF_BYTES, &tmA, full_bar(stage), kx,
-                                                 a_row + h * Cfg::MMA_M);
-                            ptx::tma_load_2d(b_dst, b_map, full_bar(stage), kx, b_row);
-                        } else {
-                            // Both CTAs' bytes complete on the leader's full barrier; the
-                            // leader announces the pair's total.
-                            const uint32_t leader_full = ptx::mapa(full_bar(stage), leader);
-                            if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * stage_bytes);
+                        for (int a = 0; a < KA; ++a) {
+                            if (a >= na) break;
+                            const uint32_t a_dst = slot_addr(stage, a);
+                            const uint32_t b_dst = a_dst + Cfg::A_BYTES;
+                            const int kx = (reverse ? (kb1 - 1 - (kb + a - kb0)) : kb + a) * kStageK;
+                            if constexpr (CG == 1) {
 #pragma unroll
-                            for (int h = 0; h < CONS; ++h)
-                                ptx::tma_load_2d_pair(a_dst + h * Cfg::A_HALF_BYTES, &tmA, leader_full, kx,
-                                                      a_row + h * Cfg::MMA_M);
-                            ptx::tma_load_2d_pair(b_dst, b_map, leader_full, kx, b_row);
+                                for (int h = 0; h < CONS; ++h)
+                                    ptx::tma_load_2d(a_dst + h * Cfg::A_HALF_BYTES, &tmA, bar, kx,
+                                                     a_row + h * Cfg::MMA_M);
+                                ptx::tma_load_2d(b_dst, b_map, bar, kx, b_row);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < CONS; ++h)
+                                    ptx::tma_load_2d_pair(a_dst + h * Cfg::A_HALF_BYTES, &tmA, bar, kx,
+                                                          a_row + h * Cfg::MMA_M);
+                                ptx::tma_load_2d_pair(b_dst, b_map, bar, kx, b_row);
+                            }
                         }
                     }
                     __syncwarp();
@@ -315,27 +324,34 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t d_tmem = tmem_base + buf * CONS * Cfg::BN;   // consumer h adds h * BN
                 // the producer's K order for this unit (odd rounds walk K downwards)
                 const bool reverse = (it & 1u) && p.ksplit == 1;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += KA) {
+                    const int na = (KA == 1 || kb1 - kb >= KA) ? KA : kb1 - kb;
                     if (!wait_phase_warp(full_bar(stage), phase, p.status, kSiteMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint64_t a_desc = ptx::sw128_kmajor_desc(sbase + stage * stride);
-                    const uint64_t b_desc = ptx::sw128_kmajor_desc(sbase + stage * stride + Cfg::A_BYTES);
-                    // the last K block holds only p.last_k_steps 32-byte steps of real
-                    // data (the rest is TMA zero fill): skip the MMAs of the others
-                    const int blk = reverse ? (kb1 - 1 - (kb - kb0)) : kb;
-                    const int steps = (blk == p.k_blocks - 1) ? p.last_k_steps : kMmaPerStage;
                     if (ptx::elect_one()) {
-                        // each consumer's MMAs read its own 128 rows of A and the shared B
 #pragma unroll
-                        for (int h = 0; h < CONS; ++h)
+                        for (int a = 0; a < KA; ++a) {
+                            if (a >= na) break;
+                            const uint64_t a_desc = ptx::sw128_kmajor_desc(slot_addr(stage, a));
+                            const uint64_t b_desc = ptx::sw128_kmajor_desc(slot_addr(stage, a) + Cfg::A_BYTES);
+                            // the last K block holds only p.last_k_steps 32-byte steps of
+                            // real data (the rest is TMA zero fill): skip the MMAs of the others
+                            const int blk = reverse ? (kb1 - 1 - (kb + a - kb0)) : kb + a;
+                            const int steps = (blk == p.k_blocks - 1) ? p.last_k_steps : kMmaPerStage;
+                            const bool first = kb == kb0 && a == 0;
+                            // each consumer's MMAs read its own 128 rows of A and the shared B
 #pragma unroll
-                            for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
-                                if (k < steps)
-                                    ptx::mma<CG, F8>(d_tmem + h * Cfg::BN, a_desc + h * (Cfg::A_HALF_BYTES >> 4) + 2u * k,
-                                                     b_desc + 2u * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                            for (int h = 0; h < CONS; ++h)
+#pragma unroll
+                                for (int k = 0; k < kMmaPerStage; ++k)   // 32 bytes of K each
+                                    if (k < steps)
+                                        ptx::mma<CG, F8>(d_tmem + h * Cfg::BN,
+                                                         a_desc + h * (Cfg::A_HALF_BYTES >> 4) + 2u * k,
+                                                         b_desc + 2u * k, idesc, (!first || k != 0) ? 1u : 0u);
+                        }
                         if constexpr (CG == 1) ptx::mma_commit(empty_bar(stage));
                         else ptx::mma_commit_pair(empty_bar(stage), pair_mask);
                     }

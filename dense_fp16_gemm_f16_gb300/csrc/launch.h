@@ -12,8 +12,9 @@ namespace gemm_gb300 {
 
 struct TiledOps {
     // tile_m: rows of one tile (per CTA pair when cta_group == 2); cluster: CTAs
-    // per cluster; b_box_rows: rows of B per TMA box (each CTA's B rows)
-    int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols, cluster, b_box_rows;
+    // per cluster; b_box_rows: rows of B per TMA box (each CTA's B rows);
+    // max_stage_atoms: the most K blocks per ring stage a launch may ask for
+    int cta_group, tile_m, tile_n, stages, smem_bytes, tmem_cols, cluster, b_box_rows, max_stage_atoms;
     // set the kernel's shared-memory limit on the current device
     cudaError_t (*prepare)();
     // co-resident clusters (cta_group 2) or CTAs per SM (cta_group 1) on the current device

@@ -8,9 +8,19 @@ namespace gemm_gb300 {
 
 template <class Cfg, class T, bool F8>
 struct TiledLauncher {
+    // 1-CTA configurations also come with two K blocks per ring stage (for
+    // launches made only of narrow column pieces)
+    static constexpr int kMaxAtoms = Cfg::CG == 1 ? 2 : 1;
+
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T, F8, 1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if constexpr (kMaxAtoms > 1) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_tiled_kernel<Cfg, T, F8, 2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        }
+        return e;
     }
 
     static cudaError_t max_active(int* out) {
@@ -72,12 +82,17 @@ struct TiledLauncher {
             cfg.numAttrs = 2;
         }
         cfg.attrs = attr;
-        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T, F8>, a, b, b_piece, d, p);
+        if constexpr (kMaxAtoms > 1) {
+            if (p.stage_atoms == 2)
+                return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T, F8, 2>, a, b, b_piece, d, p);
+        }
+        if (p.stage_atoms != 1) return cudaErrorInvalidValue;
+        return cudaLaunchKernelEx(&cfg, gemm_tiled_kernel<Cfg, T, F8, 1>, a, b, b_piece, d, p);
     }
 
     static const TiledOps& ops() {
         static const TiledOps o = {Cfg::CG, Cfg::BM, Cfg::BN, Cfg::STAGES, Cfg::SMEM_BYTES,
-                                   Cfg::TMEM_COLS, Cfg::CG, Cfg::B_ROWS,
+                                   Cfg::TMEM_COLS, Cfg::CG, Cfg::B_ROWS, kMaxAtoms,
                                    &prepare, &max_active, &max_active_split, &launch};
         return o;
     }
