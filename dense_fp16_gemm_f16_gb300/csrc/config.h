@@ -240,16 +240,15 @@ inline int choose_ksplit(int64_t tiles, const int* clusters, int64_t k_blocks) {
 // range's B rows, and the P fp32 partials are summed inside the cluster
 // through distributed shared memory.  With P = 1 a CTA may own several
 // ranges (persistent, one after the other).
-// Independent accumulators per output block of the small-M kernel.  Its MMAs
-// are narrow (N = MN <= 64), so one MMA adds into an accumulator in much less
-// time than the next MMA on the same accumulator has to wait for it; with the
-// four MMAs of a ring stage on four different accumulators they overlap, and
-// the epilogue adds the four in a fixed order.
+// Accumulators per output block of the small-M kernel: with 4, MMA k of a K
+// block adds into accumulator k (the epilogue adds the four in a fixed
+// order).  Measured on GB300: 0.1 us faster at M <= 32 (16 x 8192 x 8192,
+// fp16 and E4M3), 0.2 us slower at M = 64, where the epilogue's extra TMEM
+// reads cost more than the MMAs gain.
 #ifndef GEMM_SKINNY_ACCS
-#define GEMM_SKINNY_ACCS 4
+#define GEMM_SKINNY_ACCS 0   // 0: by MN as above
 #endif
-constexpr int kSkinnyAccs = GEMM_SKINNY_ACCS;
-static_assert(kSkinnyAccs == 1 || kSkinnyAccs == 2 || kSkinnyAccs == 4, "accumulators per block: 1, 2 or 4");
+constexpr int skinny_accs(int mn) { return GEMM_SKINNY_ACCS != 0 ? GEMM_SKINNY_ACCS : (mn <= 32 ? 4 : 1); }
 
 template <int MN_>
 struct SkinnyConfig {
@@ -266,10 +265,11 @@ struct SkinnyConfig {
     // partials received from the cluster: [P][128 columns][MN / P rows] fp32 = MN * 128 fp32
     static constexpr int RECV_BYTES = MN * 128 * 4;
     static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;
-    // Each accumulator buffer is kSkinnyAccs independent MN-column
-    // accumulators (MMA k of a stage adds into accumulator k % kSkinnyAccs),
-    // two buffers.
-    static constexpr int ACC_COLS = kSkinnyAccs * MN;
+    // Each of the two accumulator buffers is ACCS MN-column accumulators
+    // (MMA k of a K block adds into accumulator k % ACCS).
+    static constexpr int ACCS = skinny_accs(MN);
+    static_assert(ACCS == 1 || ACCS == 2 || ACCS == 4, "accumulators per block: 1, 2 or 4");
+    static constexpr int ACC_COLS = ACCS * MN;
     static constexpr int TMEM_COLS = (2 * ACC_COLS < 32) ? 32 : 2 * ACC_COLS;
     // ring = [stages B slots][stages A slots], split at run time (ring_stages)
     static constexpr int RING_BYTES = (kMaxDynSmem - 1024 - RECV_BYTES - NUM_BARS * 8 - 16) / 1024 * 1024;

@@ -40,13 +40,13 @@
 namespace gemm_gb300 {
 
 // The output block held in TMEM at `taddr` (this warp's lanes): the sum of
-// its kSkinnyAccs accumulators, added in ascending order.
-template <int MN>
+// its ACCS accumulators, added in ascending order.
+template <int MN, int ACCS>
 __device__ __forceinline__ void skinny_acc_sum(uint32_t taddr, uint32_t (&v)[MN]) {
     ptx::tmem_ld_cols<MN>(taddr, v);
     ptx::tmem_wait_ld();
 #pragma unroll
-    for (int a = 1; a < kSkinnyAccs; ++a) {
+    for (int a = 1; a < ACCS; ++a) {
         uint32_t w[MN];
         ptx::tmem_ld_cols<MN>(taddr + static_cast<uint32_t>(a * MN), w);
         ptx::tmem_wait_ld();
@@ -201,9 +201,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         const uint64_t x_desc = ptx::sw128_kmajor_desc(x_slot(stage, a));
 #pragma unroll
                         for (int k = 0; k < kMmaPerStage; ++k)
-                            ptx::mma<1, F8>(d_tmem + static_cast<uint32_t>((k % kSkinnyAccs) * MN), w_desc + 2u * k,
+                            ptx::mma<1, F8>(d_tmem + static_cast<uint32_t>((k % Cfg::ACCS) * MN), w_desc + 2u * k,
                                             x_desc + 2u * k, idesc,
-                                            (kb != kb0 || a != 0 || k >= kSkinnyAccs) ? 1u : 0u);
+                                            (kb != kb0 || a != 0 || k >= Cfg::ACCS) ? 1u : 0u);
                     }
                     ptx::mma_commit(empty_bar(stage));
                 }
@@ -238,7 +238,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 if (!wait_phase_warp(tfull_bar(buf), use, p.status, kSiteEpilogueTmemFull, p.timeout_ns)) break;
                 ptx::tc_fence_after();
                 uint32_t v[MN];
-                skinny_acc_sum<MN>(t_lane + buf * Cfg::ACC_COLS, v);
+                skinny_acc_sum<MN, Cfg::ACCS>(t_lane + buf * Cfg::ACC_COLS, v);
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
@@ -270,7 +270,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint32_t v[MN];
             if (ready) {
                 ptx::tc_fence_after();
-                skinny_acc_sum<MN>(t_lane, v);
+                skinny_acc_sum<MN, Cfg::ACCS>(t_lane, v);
             } else {
 #pragma unroll
                 for (int m = 0; m < MN; ++m) v[m] = 0u;
