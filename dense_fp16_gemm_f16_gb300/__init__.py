@@ -43,6 +43,7 @@ class Variant(enum.IntEnum):
     TILE_2CTA_SPLITK = 5
     SKINNY_STREAMK = 6
     TILE_2CTA_512x256 = 7
+    TILE_1CTA_SPLITK = 8
 
 
 class Dtype(enum.IntEnum):

@@ -58,6 +58,7 @@ struct DeviceState {
     int per_sm_1cta256 = 0;
     int skinny_clusters[kSkinnyMaxPieces + 1] = {};   // co-resident small-M clusters of P CTAs
     int split_clusters[kSplitMaxPieces + 1] = {};     // co-resident split-K clusters of S CTA pairs
+    int split1_clusters[kSplitMaxPieces1 + 1] = {};   // co-resident split-K clusters of S single CTAs
 };
 
 struct Workspace {
@@ -81,23 +82,33 @@ constexpr int64_t kMaxDim = INT32_MAX;
 // faster and 12 % less DRAM traffic than 8), 12 at 6144^3, all 16 at
 // 4000 x 11000 x 4104.  GEMM_GROUP_M fixes the group size instead.
 constexpr int64_t kL2GroupBytes = 48ll << 20;
-// AUTO's choice for shapes whose 256x256 tiles fill less than one round of CTA
-// pairs: split each tile's K loop over a cluster of S pairs when the K blocks
-// a split saves, kb * (1 - 1/S), reach kSplitKSavedBlocks.  A K block (one
-// 128-byte stage) takes a pair ~0.25 us; in back-to-back launches on GB300 a
-// split launch costs ~10 us more than an unsplit one (exchanging the fp32
+// AUTO's choice for shapes whose 256x256 pair tiles fill less than one round
+// of CTA pairs: the fastest of four plans by a small cost model, each term
+// fitted to back-to-back launches on GB300 (fp16 and E4M3, K blocks of 128
+// bytes; 14 mid shapes from 256x256x8192 to 2048x2048x2048):
+//  - 128x256 tiles on single CTAs, cut into column pieces of width w to
+//    fill the SMs (two K blocks per ring stage): kMidFixedUs + kb * t(w),
+//    t(64) = 0.20, t(128) = 0.24, t(256) = 0.40 us per K block;
+//  - whole 256x256 tiles on pairs (kb >= kPairMinBlocks): kMidFixedUs + 1 +
+//    kb * 0.33 us;
+//  - split K over a cluster of S pairs: 11.0 + ceil(kb / S) * 0.31 us;
+//  - split K over a cluster of S single CTAs (S up to 8, so a larger S fits
+//    one wave): 12.5 + ceil(kb / S) * 0.35 us.
+// A split launch costs ~10 us more than an unsplit one (exchanging the fp32
 // partials through distributed shared memory ~3 us, the cluster barriers
 // ~2 us, the slice sums and D stores ~2 us, a slower ramp and teardown).
-// Measured (fp16, us, split / unsplit pairs / 128x256 CTAs): 512x2048x8192 S=3
-// 23.8 / 32.5 / 35.3; 768x2048x6144 S=2 24.5 / 26.5 / 29.0; 1024x2048x5120 S=2
-// 23.1 / 23.4 / 25.1; 1024x1024x4096 S=3 18.0 / 19.0 / 19.7; 1024x1024x2048
-// S=3 14.7 / 12.2 / 11.9; 256x256x8192 S=4 19.1 / 32.0 / 34.7.
-constexpr int64_t kSplitKSavedBlocks = 40;
-// Unsplit, the pair kernel beats 128x256 tiles on single CTAs once the K loop
-// is long enough for its halved operand traffic per FLOP to matter (fp16
-// 1024x2048x5120: 23.3 against 25.2 us; E4M3 512x2048x8192: 19.3 against
-// 19.9); short K loops favour the single CTAs (fp16 2048^3: 14.1 against
-// 15.7 us).
+// Measured (fp16, us; unsplit 128x256 pieces / pair split / 1-CTA split):
+// 1024x1024x4096 15.6 / 18.3 / 18.0; 512x2048x8192 26.6 / 24.4 / 24.1;
+// 256x256x8192 25.8 / 19.3 / 17.3; 768x2048x6144 26.3 / 25.0 / 26.9;
+// 128x512x16384 48.1 / 28.9 / 23.9.  Against every plan forced in turn on 20
+// mid shapes, AUTO's choice was the fastest or within 2 % of it.
+constexpr double kMidFixedUs = 3.0;
+constexpr double kMidBlockUs64 = 0.20, kMidBlockUs128 = 0.24, kMidBlockUs256 = 0.40;
+constexpr double kMidPairBlockUs = 0.33;
+constexpr double kSplitPairFixedUs = 11.0, kSplitPairBlockUs = 0.31;
+constexpr double kSplit1FixedUs = 12.5, kSplit1BlockUs = 0.35;
+// Whole pair tiles enter the comparison only from this many K blocks on (their
+// halved operand traffic per FLOP pays only in long K loops).
 constexpr int64_t kPairMinBlocks = 48;
 // Even when the pair tiles fill the GPU, K loops this short (each tile mostly
 // epilogue) run faster on 128x256 CTAs.  Interleaved A/B on GB300: E4M3 with
@@ -162,13 +173,15 @@ struct Limits {
     int per_sm_1cta256;
     int skinny_clusters[kSkinnyMaxPieces + 1];   // index P: co-resident clusters of P CTAs (0: unknown)
     int split_clusters[kSplitMaxPieces + 1];     // index S: co-resident clusters of S CTA pairs
+    int split1_clusters[kSplitMaxPieces1 + 1];   // index S: co-resident clusters of S single CTAs
 };
 
 // A pure-host planner's view of a GPU with `sms` SMs (nothing queried).
 Limits host_limits(int sms) {
-    Limits lim{sms, sms / 2, sms / 2, 1, 1, {}, {}};
+    Limits lim{sms, sms / 2, sms / 2, 1, 1, {}, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; pc *= 2) lim.skinny_clusters[pc] = sms / pc;
     for (int s = 1; s <= kSplitMaxPieces; ++s) lim.split_clusters[s] = sms / (2 * s);
+    for (int s = 1; s <= kSplitMaxPieces1; ++s) lim.split1_clusters[s] = sms / s;
     return lim;
 }
 
@@ -289,10 +302,45 @@ int32_t tiled_stage_atoms(const gemm_plan_t& pl, int max_atoms) {
 const TiledOps& tiled_ops_of(gemm_variant_t v, int dtype) {
     switch (v) {
         case GEMM_VARIANT_TILE_1CTA_128x128: return tiled_ops_1cta128(dtype);
-        case GEMM_VARIANT_TILE_1CTA_128x256: return tiled_ops_1cta256(dtype);
+        case GEMM_VARIANT_TILE_1CTA_128x256:
+        case GEMM_VARIANT_TILE_1CTA_SPLITK: return tiled_ops_1cta256(dtype);
         case GEMM_VARIANT_TILE_2CTA_512x256: return tiled_ops_2cta512(dtype);
         default: return tiled_ops_2cta256(dtype);   // TILE_2CTA_256x256, TILE_2CTA_SPLITK
     }
+}
+
+// AUTO for shapes whose pair tiles fill less than one round (see kMidFixedUs).
+gemm_variant_t mid_shape_variant(int64_t M, int64_t N, int64_t kb, const Limits& lim) {
+    const int64_t t1 = cdiv(M, 128) * cdiv(N, 256);
+    const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
+    const double k = static_cast<double>(kb);
+    // 128x256 tiles on single CTAs, the last round cut into column pieces
+    const int per256 = lim.per_sm_1cta256 > 0 ? lim.per_sm_1cta256 : 1;
+    const int64_t slots1 = static_cast<int64_t>(lim.sms) * per256;
+    int64_t full1;
+    int split1;
+    tail_split(t1, slots1, 256, 1, full1, split1);
+    const double per_block = split1 == 4 ? kMidBlockUs64 : (split1 == 2 ? kMidBlockUs128 : kMidBlockUs256);
+    const int64_t rounds1 = cdiv(full1, slots1) + cdiv((t1 - full1) * split1, slots1);
+    double best = kMidFixedUs + static_cast<double>(rounds1) * k * per_block;
+    gemm_variant_t v = t1 >= 2 ? GEMM_VARIANT_TILE_1CTA_128x256 : GEMM_VARIANT_TILE_1CTA_128x128;
+    // whole pair tiles, long K loops
+    if (kb >= kPairMinBlocks) {
+        const double t = kMidFixedUs + 1.0 + k * kMidPairBlockUs;
+        if (t < best) { best = t; v = GEMM_VARIANT_TILE_2CTA_256x256; }
+    }
+    // split K over pairs, or over single CTAs
+    const int s2 = choose_ksplit(t2, lim.split_clusters, kb);
+    if (s2 > 1) {
+        const double t = kSplitPairFixedUs + static_cast<double>(cdiv(kb, s2)) * kSplitPairBlockUs;
+        if (t < best) { best = t; v = GEMM_VARIANT_TILE_2CTA_SPLITK; }
+    }
+    const int s1 = choose_ksplit(t1, lim.split1_clusters, kb, kSplitMaxPieces1);
+    if (s1 > 1) {
+        const double t = kSplit1FixedUs + static_cast<double>(cdiv(kb, s1)) * kSplit1BlockUs;
+        if (t < best) { best = t; v = GEMM_VARIANT_TILE_1CTA_SPLITK; }
+    }
+    return v;
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant, const Limits& lim,
@@ -301,7 +349,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     const gemm_status_t st = check_sizes(M, N, K, in_bytes);
     if (st != GEMM_OK) return st;
     const int64_t bk = stage_k(in_bytes);
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_512x256) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_1CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
         return GEMM_ERR_INVALID_VALUE;
     if (lim.sms <= 0) return GEMM_ERR_INVALID_VALUE;
@@ -312,29 +360,20 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
             variant = GEMM_VARIANT_SKINNY_SPLITK;
         } else {
             // The pair kernel when its 256x256 tiles fill at least one round of
-            // CTA pairs; below that, 128x256 tiles on single CTAs (twice as many
-            // units for the same shape); a single 128x128 tile for the smallest.
-            // (Measured on GB300: e.g. 2048^3 14.1 us on 128x256 vs 15.7 us on
-            // pairs and 20.3 us on 128x128; 4000x11000x4104 253 us on pairs vs
-            // 350 us on 128x256.)
-            // With at most half a round of pair tiles and a long K loop, split
-            // each tile's K loop over several pairs instead (see
-            // kSplitKSavedBlocks); unsplit, long K loops go to the pair kernel
-            // and short ones to single CTAs (kPairMinBlocks).
+            // CTA pairs (4000x11000x4104: 253 us on pairs vs 350 us on 128x256
+            // CTAs), with the exceptions below; under one round, the cost
+            // model of mid_shape_variant (128x256 column pieces on single
+            // CTAs, whole pair tiles, or split K over pairs or single CTAs).
             const int64_t t2 = cdiv(M, 256) * cdiv(N, 256);
             const int64_t kb = cdiv(K, bk);
-            const int ks = choose_ksplit(t2, lim.split_clusters, kb);
             if (t2 >= pairs && kb <= (in_bytes == 1 ? kShortKBlocks8 : kShortKBlocks16))
                 variant = GEMM_VARIANT_TILE_1CTA_128x256;
             else if (t2 >= pairs && (K * in_bytes) % 32 != 0 && cdiv(M, 512) * cdiv(N, 256) >= 2 * pairs)
                 variant = GEMM_VARIANT_TILE_2CTA_512x256;
             else if (t2 >= pairs)
                 variant = GEMM_VARIANT_TILE_2CTA_256x256;
-            else if (ks > 1 && kb * (ks - 1) >= kSplitKSavedBlocks * ks)
-                variant = GEMM_VARIANT_TILE_2CTA_SPLITK;
-            else if (kb >= kPairMinBlocks) variant = GEMM_VARIANT_TILE_2CTA_256x256;
-            else if (cdiv(M, 128) * cdiv(N, 256) >= 2) variant = GEMM_VARIANT_TILE_1CTA_128x256;
-            else variant = GEMM_VARIANT_TILE_1CTA_128x128;
+            else
+                variant = mid_shape_variant(M, N, kb, lim);
         }
     }
     pl->variant = variant;
@@ -394,8 +433,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     if (variant == GEMM_VARIANT_TILE_2CTA_SPLITK &&
         choose_ksplit(cdiv(M, 256) * cdiv(N, 256), lim.split_clusters, pl->k_blocks) < 2)
         variant = GEMM_VARIANT_TILE_2CTA_256x256;   // too many tiles for one wave of clusters: no split
+    if (variant == GEMM_VARIANT_TILE_1CTA_SPLITK &&
+        choose_ksplit(cdiv(M, 128) * cdiv(N, 256), lim.split1_clusters, pl->k_blocks, kSplitMaxPieces1) < 2)
+        variant = GEMM_VARIANT_TILE_1CTA_128x256;
     pl->variant = variant;
-    const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK;
+    const bool ksplit_variant = variant == GEMM_VARIANT_TILE_2CTA_SPLITK || variant == GEMM_VARIANT_TILE_1CTA_SPLITK;
     const TiledOps& ops = tiled_ops_of(variant, 0);
     pl->cta_group = ops.cta_group;
     pl->tile_m = ops.tile_m;
@@ -422,8 +464,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_variant_t variant,
     int ksplit = 1;
     int64_t clusters;
     if (ksplit_variant) {
-        // one cluster of ksplit pairs per tile, all resident in one wave
-        ksplit = choose_ksplit(tiles, lim.split_clusters, pl->k_blocks);
+        // one cluster of ksplit MMA groups per tile, all resident in one wave
+        ksplit = variant == GEMM_VARIANT_TILE_1CTA_SPLITK
+                     ? choose_ksplit(tiles, lim.split1_clusters, pl->k_blocks, kSplitMaxPieces1)
+                     : choose_ksplit(tiles, lim.split_clusters, pl->k_blocks);
         num_full = tiles;
         split = 1;
         clusters = tiles;
@@ -519,6 +563,13 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
                 d.split_clusters[sp] = 0;
             }
         }
+        d.split1_clusters[1] = sms * per256;
+        for (int sp = 2; sp <= kSplitMaxPieces1; ++sp) {
+            if (tiled[2]->max_active_split(sp, &d.split1_clusters[sp]) != cudaSuccess) {
+                cudaGetLastError();
+                d.split1_clusters[sp] = 0;
+            }
+        }
         d.ready = true;
     }
     *out = &d;
@@ -527,9 +578,10 @@ gemm_status_t get_device(DeviceState** out, int* dev_out) {
 }
 
 Limits limits_of(const DeviceState& d) {
-    Limits lim{d.sms, d.max_clusters_2cta, d.max_clusters_2cta2c, d.per_sm_1cta128, d.per_sm_1cta256, {}, {}};
+    Limits lim{d.sms, d.max_clusters_2cta, d.max_clusters_2cta2c, d.per_sm_1cta128, d.per_sm_1cta256, {}, {}, {}};
     for (int pc = 1; pc <= kSkinnyMaxPieces; ++pc) lim.skinny_clusters[pc] = d.skinny_clusters[pc];
     for (int sp = 1; sp <= kSplitMaxPieces; ++sp) lim.split_clusters[sp] = d.split_clusters[sp];
+    for (int sp = 1; sp <= kSplitMaxPieces1; ++sp) lim.split1_clusters[sp] = d.split1_clusters[sp];
     return lim;
 }
 
@@ -672,7 +724,7 @@ gemm_status_t run(const void* A, const void* B, void* D, int64_t M, int64_t N, i
             if (epi.scale_n && ranges_overlap(epi.scale_n, N * 4, D, M * N * 2)) return GEMM_ERR_INVALID_VALUE;
         }
     }
-    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_2CTA_512x256) return GEMM_ERR_INVALID_VALUE;
+    if (variant < GEMM_VARIANT_AUTO || variant > GEMM_VARIANT_TILE_1CTA_SPLITK) return GEMM_ERR_INVALID_VALUE;
     if ((variant == GEMM_VARIANT_SKINNY_SPLITK || variant == GEMM_VARIANT_SKINNY_STREAMK) && M > 64)
         return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;

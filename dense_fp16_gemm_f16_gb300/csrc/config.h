@@ -212,19 +212,31 @@ inline void tail_split(int64_t num_tiles, int64_t slots, int BN, int CG, int64_t
     }
 }
 
-// Split-K factor for the pair kernel (clusters of S pairs, S <= 4 so that a
-// cluster has at most the 8 CTAs every GPU of this class supports): the most
-// pieces such that every tile's cluster is resident in one wave
-// (tiles <= clusters[S], the co-resident clusters of S pairs) and every piece
-// keeps at least kSplitMinBlocks K blocks; 1 = no split.
-constexpr int kSplitMaxPieces = 4;
+// Split-K factor S (a cluster of S MMA groups per tile: S pairs, S <= 4, or S
+// single CTAs, S <= 8, so that a cluster has at most the 8 CTAs every GPU of
+// this class supports): the most pieces such that every tile's cluster is
+// resident in one wave (tiles <= clusters[S], the co-resident clusters of S
+// groups) and every piece keeps at least kSplitMinBlocks K blocks; 1 = no
+// split.
+constexpr int kSplitMaxPieces = 4;      // pairs
+constexpr int kSplitMaxPieces1 = 8;     // single CTAs
 constexpr int64_t kSplitMinBlocks = 4;
-inline int choose_ksplit(int64_t tiles, const int* clusters, int64_t k_blocks) {
+// Bytes of the split-K receive buffer ([S][2 ceil(bn/8 / S)][128 rows][16 B],
+// kernel_tiled.cuh), which reuses the operand ring, and whether every S up to
+// max_s fits a ring of ring_bytes.
+GEMM_HD constexpr int split_recv_bytes(int bn, int s) { return s * 2 * ((bn / 8 + s - 1) / s) * 128 * 16; }
+GEMM_HD constexpr bool split_recv_fits(int bn, int ring_bytes, int max_s) {
+    for (int s = 2; s <= max_s; ++s)
+        if (split_recv_bytes(bn, s) > ring_bytes) return false;
+    return true;
+}
+
+inline int choose_ksplit(int64_t tiles, const int* clusters, int64_t k_blocks, int max_pieces = kSplitMaxPieces) {
 #ifdef GEMM_SPLIT_PIECES
     // a build that fixes S (waves of clusters allowed), for measurements
     if (tiles > 0 && k_blocks >= kSplitMinBlocks * GEMM_SPLIT_PIECES) return GEMM_SPLIT_PIECES;
 #endif
-    for (int s = kSplitMaxPieces; s >= 2; --s)
+    for (int s = max_pieces; s >= 2; --s)
         if (tiles > 0 && tiles <= clusters[s] && k_blocks >= kSplitMinBlocks * s) return s;
     return 1;
 }

@@ -151,6 +151,8 @@ gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                   const TiledParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int CONS = Cfg::CONS;
+    static_assert(split_recv_fits(Cfg::BN, Cfg::RING_BYTES, CG == 2 ? kSplitMaxPieces : kSplitMaxPieces1),
+                  "the split-K receive buffer must fit the operand ring");
     constexpr int MAXS = Cfg::MAX_STAGES;
     constexpr int kStageK = stage_k(F8 ? 1 : 2);
     extern __shared__ uint8_t smem_raw[];

@@ -95,9 +95,13 @@ typedef enum {
                                            in equal contiguous ranges to all SMs, split tiles
                                            summed through the fp32 workspace (the kernel of
                                            gemm_f16_nt_noalloc) */
-    GEMM_VARIANT_TILE_2CTA_512x256 = 7  /* persistent, 2-CTA cluster, 512x256 tile per pair: two
+    GEMM_VARIANT_TILE_2CTA_512x256 = 7, /* persistent, 2-CTA cluster, 512x256 tile per pair: two
                                            MMA consumers per CTA share each staged B tile, each
                                            with its own accumulator and epilogue warpgroup */
+    GEMM_VARIANT_TILE_1CTA_SPLITK = 8   /* 1-CTA 128x256 tiles with each tile's K loop split over
+                                           a cluster of up to 8 CTAs (for shapes with few tiles);
+                                           falls back to GEMM_VARIANT_TILE_1CTA_128x256 when the
+                                           tiles already fill the GPU */
 } gemm_variant_t;
 
 /* Element type of A and B; both operands share it and the MMA accumulates in

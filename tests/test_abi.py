@@ -64,7 +64,7 @@ def test_argument_errors_are_returned_before_any_device_call(lib):
     assert _call(8, -8, 8) == S.ERR_INVALID_VALUE
     assert _call(8, 8, -8) == S.ERR_INVALID_VALUE
     assert _call(2 ** 31, 8, 8) == S.ERR_INVALID_VALUE
-    assert _call(8, 8, 8, variant=8) == S.ERR_INVALID_VALUE
+    assert _call(8, 8, 8, variant=9) == S.ERR_INVALID_VALUE
     assert _call(65, 8, 8, variant=g.Variant.SKINNY_SPLITK) == S.ERR_INVALID_VALUE
     assert _call(65, 8, 8, variant=g.Variant.SKINNY_STREAMK) == S.ERR_INVALID_VALUE
     # empty problems are a no-op even with NULL pointers
@@ -276,11 +276,24 @@ def test_ksplit_choice(lib):
     assert q["k_split"] == 3 and q["grid_ctas"] == 2 * 20 * 3
     q = P(256 * 8, 256 * 5, 64 * 64, variant=V)                           # 40 tiles: too many for one wave
     assert q["variant"] == "TILE_2CTA_256x256" and q["k_split"] == 1
-    # AUTO splits only where the K blocks a split saves, kb * (1 - 1/S), reach 40
-    assert P(256, 256, 64 * 53)["k_split"] == 1 and P(256, 256, 64 * 54)["k_split"] == 4
-    assert P(1024, 2048, 64 * 78)["variant"] == "TILE_2CTA_256x256"     # S = 2 saves 39 blocks: unsplit
-    assert P(1024, 2048, 64 * 80)["k_split"] == 2                         # S = 2 saves 40 blocks: split
-    assert P(768, 2048, 64 * 96)["k_split"] == 3                          # 24 tiles: 25 clusters of 3 pairs fit
+    # single CTAs: up to 8 pieces per tile (clusters of up to 8 CTAs; 152 SMs: 152 / S clusters)
+    V1 = g.Variant.TILE_1CTA_SPLITK
+    assert P(128, 256, 64 * 64, variant=V1)["k_split"] == 8
+    assert P(128, 256, 64 * 20, variant=V1)["k_split"] == 5               # >= 4 K blocks a piece
+    q = P(128 * 20, 256, 64 * 64, variant=V1)                             # 20 tiles: 21 clusters of 7 fit
+    assert q["k_split"] == 7 and q["grid_ctas"] == 20 * 7 and q["cta_group"] == 1
+    assert P(128 * 40, 256, 64 * 64, variant=V1)["k_split"] == 3
+    q = P(128 * 160, 256, 64 * 64, variant=V1)                            # 160 tiles: no wave fits
+    assert q["variant"] == "TILE_1CTA_128x256" and q["k_split"] == 1
+    # AUTO below one round of pair tiles: the cheapest of unsplit column pieces on
+    # single CTAs, whole pair tiles, split K over pairs or over single CTAs
+    assert P(256, 256, 64 * 20)["variant"] == "TILE_1CTA_128x256"        # short K: no split
+    assert P(256, 256, 64 * 128)["variant"] == "TILE_1CTA_SPLITK"        # 2 tiles, long K: 8 pieces each
+    assert P(256, 256, 64 * 128)["k_split"] == 8
+    assert P(1024, 2048, 64 * 80)["variant"] == "TILE_1CTA_128x256"      # 64 tiles in halves beat S = 2
+    q = P(768, 2048, 64 * 96)                                             # 24 tiles: 25 clusters of 3 pairs fit
+    assert q["variant"] == "TILE_2CTA_SPLITK" and q["k_split"] == 3
+    assert P(2048, 2048, 64 * 128)["variant"] == "TILE_2CTA_256x256"     # 64 whole pair tiles, long K
 
 
 def test_plans_for_8bit_operands(lib):
@@ -300,10 +313,10 @@ def test_plans_for_8bit_operands(lib):
         P(4000, 11000, 4104)                                 # 4104-byte rows: not 16-byte units
     p = P(16, 8192, 8192)
     assert p["variant"] == "SKINNY_SPLITK" and p["k_blocks"] == 64 and (p["k_split"], p["n_tiles"]) == (2, 76)
-    p = P(512, 2048, 8192)                                   # 16 pair tiles, 64 K blocks: a split by 4
-    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4      # saves 48 blocks: split
-    p = P(512, 1024, 16384)                                  # 128 K blocks over 4 pieces: split
-    assert p["variant"] == "TILE_2CTA_SPLITK" and p["k_split"] == 4
+    p = P(512, 2048, 8192)                                   # 64 K blocks: 128 column pieces beat a split
+    assert p["variant"] == "TILE_1CTA_128x256" and p["tail_split"] == 4
+    p = P(512, 1024, 16384)                                  # 128 K blocks: 16 single-CTA tiles in 8 pieces
+    assert p["variant"] == "TILE_1CTA_SPLITK" and p["k_split"] == 8
     assert g.gemm_nt_plan_ex(g.Dtype.F16, 8192, 8192, 8192, num_sms=152) == \
         g.gemm_f16_nt_plan(8192, 8192, 8192, num_sms=152)
     assert g.gemm_nt_plan_ex(g.Dtype.E5M2, 8192, 8192, 8192, num_sms=152)["tile_k"] == 128

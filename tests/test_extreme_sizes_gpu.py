@@ -70,12 +70,14 @@ def test_a_million_k_small_m():
     check_close(D.cpu().numpy(), oracle.gemm(A, B), K, "K = 2^20, small M")
 
 
-def test_long_k_split_pairs():
-    M, N, K = 256, 264, (1 << 18) + 8         # ragged N and K; the pair tiles' K loops split 4 ways
-    plan = g.gemm_f16_nt_plan(M, N, K)
-    assert plan["variant"] == "TILE_2CTA_SPLITK" and plan["k_split"] == 4, plan
+@pytest.mark.parametrize("variant,pieces", [(g.Variant.TILE_2CTA_SPLITK, 4), (g.Variant.TILE_1CTA_SPLITK, 8)],
+                         ids=["pairs", "single_ctas"])
+def test_long_k_split(variant, pieces):
+    M, N, K = 256, 264, (1 << 18) + 8         # ragged N and K; every tile's K loop split 4 or 8 ways
+    plan = g.gemm_f16_nt_plan(M, N, K, variant)
+    assert plan["variant"] == variant.name and plan["k_split"] == pieces, plan
     A, B = inputs.operands(M, N, K, seed=86)
-    D = _run(A, B)
+    D = _run(A, B, variant)
     rows, cols = inputs.sample_entries(M, N, seed=87, n_rows=2, n_cols=2, n_random=2048,
                                        extra_rows=[M - 1], extra_cols=[N - 1, N - 8, 255, 256])
     _sampled(D, A, B, K, "K = 2^18 + 8, split pairs", rows, cols)

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256,
-         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]
+         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256, g.Variant.TILE_1CTA_SPLITK]
 
 
 @pytest.fixture(scope="module", autouse=True)

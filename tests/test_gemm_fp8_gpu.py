@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256,
-         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]
+         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256, g.Variant.TILE_1CTA_SPLITK]
 DT = {"e4m3": g.Dtype.E4M3, "e5m2": g.Dtype.E5M2}
 
 

@@ -91,7 +91,7 @@ def test_named_workload_sampled(name):
 
 # ---------------------------------------------------------------- every variant, ragged
 TILED = [g.Variant.TILE_2CTA_256x256, g.Variant.TILE_1CTA_128x128, g.Variant.TILE_1CTA_128x256,
-         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256]
+         g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_2CTA_512x256, g.Variant.TILE_1CTA_SPLITK]
 RAGGED = [(1, 8, 8), (7, 24, 40), (128, 128, 64), (129, 136, 72), (255, 264, 200),
           (300, 520, 1000), (513, 256, 4104), (640, 1000, 520)]
 SKINNY = [(1, 8, 8), (5, 136, 64), (16, 128, 64), (17, 200, 72), (33, 1000, 520),
@@ -142,20 +142,33 @@ def test_skinny_cluster_sizes(shape):
 @pytest.mark.parametrize("shape", [(300, 520, 1000), (513, 256, 4104), (1000, 1000, 640), (1024, 1024, 2048),
                                    (512, 2048, 8192), (272, 2056, 520), (1200, 1000, 1000), (1200, 704, 1400),
                                    (1100, 504, 2000), (300, 8, 4096)], ids=lambda s: "x".join(map(str, s)))
-def test_tile_split_k(shape):
+@pytest.mark.parametrize("variant", [g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_1CTA_SPLITK], ids=lambda v: v.name)
+def test_tile_split_k(shape, variant):
     # the planner really splits these (k_split > 1); ragged M, N and K included
     M, N, K = shape
-    plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.TILE_2CTA_SPLITK)
-    assert plan["variant"] == "TILE_2CTA_SPLITK" and plan["k_split"] > 1, plan
+    plan = g.gemm_f16_nt_plan(M, N, K, variant)
+    assert plan["variant"] == variant.name and plan["k_split"] > 1, plan
     A, B = inputs.operands(M, N, K, seed=3000 + M + N + K)
-    _full_parity(A, B, g.Variant.TILE_2CTA_SPLITK)
+    _full_parity(A, B, variant)
 
 
-def test_tile_split_k_consecutive_calls():
-    # each call re-arms its tile counters; three calls in a row, new data each time
+@pytest.mark.parametrize("variant", [g.Variant.TILE_2CTA_SPLITK, g.Variant.TILE_1CTA_SPLITK], ids=lambda v: v.name)
+def test_tile_split_k_consecutive_calls(variant):
+    # three calls in a row, new data each time
     for seed in (1, 2, 3):
         A, B = inputs.operands(700, 1000, 3000, seed=seed)
-        _full_parity(A, B, g.Variant.TILE_2CTA_SPLITK, what=f"split-K seed {seed}")
+        _full_parity(A, B, variant, what=f"split-K seed {seed}")
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 8192), (130, 264, 4104), (128, 512, 16384)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tile_split_k_single_ctas_up_to_8(shape):
+    # few 128x256 tiles and a long K loop: clusters of up to 8 single CTAs
+    M, N, K = shape
+    plan = g.gemm_f16_nt_plan(M, N, K, g.Variant.TILE_1CTA_SPLITK)
+    assert plan["variant"] == "TILE_1CTA_SPLITK" and plan["k_split"] >= 5, plan
+    A, B = inputs.operands(M, N, K, seed=3100 + M + N + K)
+    _full_parity(A, B, g.Variant.TILE_1CTA_SPLITK)
 
 
 @pytest.mark.parametrize("shape", [(96, 512, 2048), (200, 304, 4104)], ids=str)
