@@ -461,7 +461,7 @@ def time_workload(args, g, lib, dev, stream, w, peaks) -> dict:
     headline is: warm-up launches, then back-to-back launches between one CUDA
     event pair on the launch stream, operands rotated past L2."""
     import torch
-    A_h, B_h = inputs.workload_operands(w.name)
+    A_h, B_h = inputs.operands(w.M, w.N, w.K, w.dist_a, w.dist_b, w.seed)
     A, B = torch.from_numpy(A_h).to(dev), torch.from_numpy(B_h).to(dev)
     D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     ptrs, keep = rotated_copies(torch, dev, A, B)
@@ -662,13 +662,15 @@ def run_ours(args):
         e2e = run_e2e(args, w, g, lib, dev, stream, pg, world, to_torch, tdt, dtype_code, A_h, B_h, C_h, bias_h,
                       alpha, b_scale_h)
 
-    # the other named workloads (fp16 plain product), same timing rules
+    # the other named workloads (fp16 plain product), same timing rules, and one
+    # mid shape whose few tiles and long K loop take the split-K path
     configs = None
     if (not args.no_configs and rank == 0 and not args.shape and args.workload == inputs.HEADLINE
             and args.dtype == "f16" and not args.epilogue):
         peaks_c = measured_peaks()
-        configs = {name: time_workload(args, g, lib, dev, stream, wl, peaks_c)
-                   for name, wl in inputs.WORKLOADS.items() if name != inputs.HEADLINE}
+        extra = [inputs.Workload("split_k_512x2048x8192", 512, 2048, 8192, "uniform", "uniform", 6)]
+        configs = {wl.name: time_workload(args, g, lib, dev, stream, wl, peaks_c)
+                   for wl in list(inputs.WORKLOADS.values()) + extra if wl.name != inputs.HEADLINE}
 
     clocks = sampler.stop() if sampler else None
     if pg:
